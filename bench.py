@@ -1,0 +1,441 @@
+"""Benchmark: MoE expert-parallel layout + dispatch + combine on one GB300.
+
+One step = ep_get_layout -> ep_dispatch (bf16) -> ep_combine (weighted, identity
+experts: y = recv_x) over the DeepSeek-V3-shaped workload: R=8 virtual ranks x 4096
+tokens, hidden 7168 bf16, 256 experts (32 per rank), top-8 distinct uniform, fp32
+softmax weights, 12 channels, receive regions sized for the worst case (no host sync).
+
+Prints one JSON line. `value` is the effective HBM bandwidth of the whole step
+(algorithmic bytes of layout + dispatch + combine / device time per step, inputs
+resident in HBM, inputs larger than L2). `dispatch_gbs`, `combine_gbs` and
+`layout_dispatch_us` are the per-kernel figures of the same timed region, measured with
+CUDA events on the launching stream. `e2e` is the same metric through the same C-ABI
+calls with host buffers: pinned host -> device copy of x / topk_idx / topk_weights and
+a device -> host copy of the combined output inside every timed step.
+
+--impl reference times the CPU oracle (test infrastructure; single-threaded C) on a
+bounded token sample of the same workload and prints the same metric.
+
+Multi-GPU: the path does not shard (virtual ranks live in one GPU's memory), so
+`--gpus N` under torchrun runs N independent replicas; the barrier and max-over-ranks
+timing keep the contract and `value` sums all replicas' bytes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "dispatch/combine effective HBM GB/s (% of GB300 peak); µs per layout+dispatch"
+WORKLOAD = workloads.CONFIGS["dsv3"]
+BAD_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+# ----------------------------------------------------------------------------- bytes model
+
+def algorithmic_bytes(R, T, H, k, N, weighted=True):
+    """Bytes that must be read + written once (bf16 payload, int64 topk_idx, fp32
+    weights, int32 send_head / src_idx, uint8 is_token_in_rank). N = received rows."""
+    Tt = R * T
+    layout = Tt * k * 8 + Tt * R * (1 + 4)
+    dispatch = Tt * H * 2 + N * H * 2 + Tt * (k * 12 + R * 4) + N * (k * 12 + 4)
+    combine = N * H * 2 + Tt * H * 2 + Tt * R * 4 + (Tt * k * 12 if weighted else 0)
+    return {"layout": layout, "dispatch": dispatch, "combine": combine}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "combine_layout_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    with open(os.path.join(ROOT, "include", "ep.h"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        entries = json.load(f)
+    e = entries.get(kernel)
+    if not e or e.get("source_sha256") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            return
+        self.first = threading.Event()
+        self.active = False
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        self.first.wait(timeout=10)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.first.set()
+            if self.active:
+                self.lines.append(line.strip())
+
+    def start(self):
+        self.active = True
+
+    def stop(self) -> dict:
+        self.active = False
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our path
+
+def run_ours(args, rank, world):
+    import torch
+    import combine_layout_02_gb300 as ep
+    from combine_layout_02_gb300.buffers import LayoutBuffers, RecvBuffers, worst_case_row_offsets
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    ep.lib()                                              # fails loudly without libep.so
+    w = WORKLOAD
+    R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
+    inp = workloads.make_workload(w)
+    sh = ep.make_shape(R, T, H, E, k, C)
+
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(inp["topk_idx"]).to(dev)
+    wts = torch.from_numpy(inp["topk_weights"]).to(dev)
+    off = worst_case_row_offsets(R, T)
+    lb = LayoutBuffers(sh, dev)
+    rb = RecvBuffers(off[-1], H, k, device=dev)
+    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    launch = ep.make_launch(stream, error_flags=err)
+    layout_s, handle = lb.layout(), lb.handle(rb.recv_src_idx)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ep.ep_get_layout(sh, topk, layout_s, handle, lb.workspace, launch)
+        if ev is not None:
+            ev[1].record(stream)
+        ep.ep_dispatch(sh, x, ep.EP_BF16, None, ep.EP_BF16, topk, wts, handle, rb.recv_x, None,
+                       rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx, off, launch)
+        if ev is not None:
+            ev[2].record(stream)
+        ep.ep_combine(sh, rb.recv_x, off, handle, ep.EP_COMBINE_WEIGHTED, topk, wts, None, out,
+                      None, launch)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    N = int(lb.rank_prefix_matrix[-1].sum().item())
+    nbytes = algorithmic_bytes(R, T, H, k, N)
+    total_bytes = sum(nbytes.values())
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def timed_region(sampler):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize()
+        n0 = ep.ep_kernel_launch_count()
+        if sampler:
+            sampler.start()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        barrier()
+        launches = ep.ep_kernel_launch_count() - n0
+        total_ms = t_start.elapsed_time(t_end)
+        lay = [e[0].elapsed_time(e[1]) for e in evs]
+        dis = [e[1].elapsed_time(e[2]) for e in evs]
+        com = [e[2].elapsed_time(e[3]) for e in evs]
+        return total_ms, lay, dis, com, launches, clocks
+
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    gpu_id = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
+    remeasured = False
+    total_ms, lay, dis, com, launches, clocks = timed_region(ClockSampler(gpu_id))
+    if clocks and any(r in clocks["reasons"] for r in BAD_REASONS):
+        remeasured = True
+        total_ms, lay, dis, com, launches, clocks = timed_region(ClockSampler(gpu_id))
+
+    ms_step = total_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    flags = int(err.item())
+    if flags != 0:
+        raise RuntimeError(f"device error flags set: {flags}")
+
+    # ---- end to end through the C ABI with host buffers
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_h.copy_(x)
+    topk_h = torch.empty(topk.shape, dtype=topk.dtype, pin_memory=True)
+    topk_h.copy_(topk)
+    wts_h = torch.empty(wts.shape, dtype=wts.dtype, pin_memory=True)
+    wts_h.copy_(wts)
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        topk.copy_(topk_h, non_blocking=True)
+        wts.copy_(wts_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = x_h.numel() * x_h.element_size() + topk_h.numel() * 8 + wts_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+
+    peak, peak_kind = measured_peaks()
+    dis_ms = statistics.mean(dis)
+    com_ms = statistics.mean(com)
+    lay_ms = statistics.mean(lay)
+    dis_gbs = nbytes["dispatch"] / (dis_ms * 1e6)
+    com_gbs = nbytes["combine"] / (com_ms * 1e6)
+    if dis_ms >= com_ms:
+        dom, dom_gbs, dom_kernel = "dispatch", dis_gbs, "dispatch_kernel<copy>"
+    else:
+        dom, dom_gbs, dom_kernel = "combine", com_gbs, "combine_kernel"
+    value = world * total_bytes / (ms_step * 1e6)
+    result = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "dsv3: R=8 virtual ranks x 4096 tokens, hidden 7168 bf16, "
+                               "256 experts (32/rank), top-8 distinct uniform, fp32 softmax "
+                               "weights, 12 channels; layout + bf16 dispatch + weighted bf16 "
+                               "combine (identity experts), worst-case receive capacity",
+                   "R": R, "T": T, "H": H, "E": E, "k": k, "C": C, "recv_rows": N,
+                   "parallelism": f"replicas x{world} (virtual EP8 inside each GPU)",
+                   "l2": "inputs larger than L2 (x 470 MB, recv_x 2.49 GB); no flush"},
+        "dispatch_gbs": round(dis_gbs, 1),
+        "combine_gbs": round(com_gbs, 1),
+        "dispatch_frac_of_peak": round(dis_gbs / peak, 4),
+        "combine_frac_of_peak": round(com_gbs / peak, 4),
+        "layout_us": round(lay_ms * 1e3, 2),
+        "dispatch_us": round(dis_ms * 1e3, 2),
+        "combine_us": round(com_ms * 1e3, 2),
+        "layout_dispatch_us": round((lay_ms + dis_ms) * 1e3, 2),
+        "bytes_per_step": nbytes,
+        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(dom_gbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
+                     "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "traffic": traffic_from_profiles(dom_kernel),
+                     "algorithmic_bytes_per_launch": nbytes[dom]},
+        "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "clocks_remeasured": remeasured,
+    }
+    return result, inp
+
+
+# ----------------------------------------------------------------------------- oracle
+
+def oracle_sample(inp, steps: int, budget_s: float):
+    """Times the CPU oracle (layout + dispatch + weighted combine) on the first T_s tokens
+    of every source rank, T_s chosen by a short calibration so that `steps` steps take
+    about budget_s seconds. Returns (GB/s, description, seconds per step)."""
+    import oracle
+    w = WORKLOAD
+
+    def one(Ts):
+        topk = np.ascontiguousarray(inp["topk_idx"][:, :Ts])
+        wts = np.ascontiguousarray(inp["topk_weights"][:, :Ts])
+        x = np.ascontiguousarray(inp["x"][:, :Ts])
+        t0 = time.perf_counter()
+        lay = oracle.layout(topk, w.E, w.C)
+        n = lay["rank_prefix_matrix"][-1]
+        off = np.concatenate([[0], np.cumsum(n)]).astype(np.int64)
+        d = oracle.dispatch(x, lay["send_head"], off, w.E, topk, wts)
+        oracle.combine(d["recv_x"], lay["send_head"], off, w.E, w.k, oracle.COMBINE_WEIGHTED, topk, wts)
+        dt = time.perf_counter() - t0
+        return dt, int(off[-1])
+
+    cal_T = 32
+    dt, _ = one(cal_T)
+    per_tok = dt / cal_T
+    Ts = int(max(8, min(w.T, budget_s / max(steps, 1) / per_tok)))
+    times, N = [], 0
+    for _ in range(max(steps, 1)):
+        dt, N = one(Ts)
+        times.append(dt)
+    sec = statistics.mean(times)
+    b = algorithmic_bytes(w.R, Ts, w.H, w.k, N)
+    gbs = sum(b.values()) / (sec * 1e9)
+    desc = (f"first {Ts} of {w.T} tokens of each of the {w.R} source ranks of the same seeded "
+            f"workload ({N} received rows), {len(times)} step(s), single-threaded C oracle")
+    return gbs, desc, sec
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    inp = workloads.make_workload(WORKLOAD)
+    gbs, desc, sec = oracle_sample(inp, args.steps, budget_s=float(os.environ.get("EP_ORACLE_BUDGET_S", 90)))
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "dsv3 (token sample, see cpu_baseline.sample)", "R": WORKLOAD.R,
+                   "T": WORKLOAD.T, "H": WORKLOAD.H, "E": WORKLOAD.E, "k": WORKLOAD.k, "C": WORKLOAD.C},
+        "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        # The oracle runs on rank 0's host cores only; other ranks exit without work.
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend)
+
+    res, inp = run_ours(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, desc, _ = oracle_sample(inp, 2, budget_s=20.0)
+        res["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": 1,
+                               "kind": "oracle", "sample": desc}
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+// combine.cu -- normal-mode combine: rows come back from every virtual rank a token
+// was sent to and are reduced into token order.
+//
+// [README] "DeepEP" README (EnflameTechnology/DeepEP), normal-kernel example:
+//          combine_forward = combine(x, handle) -> combined_x; dispatch_backward =
+//          combine(grad_recv_x, handle, topk_weights=grad_recv_topk_weights), which
+//          also reduces the weight gradients.
+// [REUSE]  "How DeepEP Optimizes Handle Reuse for Repeated Dispatches", "Combining
+//          with Handle Reuse".
+//
+// One warp per output token: the warp gathers the destination rows from send_head
+// (ascending rank order) and their coefficients (1, or the sum of the token's weights
+// whose experts live on that rank), then accumulates in fp32 registers and stores
+// bf16 once. Each received row is read exactly once.
+#include "rowops.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct CombineArgs {
+    const char* y;
+    RowOffsets off;
+    const int32_t* send_head;
+    const int64_t* topk_idx;
+    const float* topk_weights;
+    const float* recv_topk_weights;
+    char* out;
+    float* combined_topk_weights;
+    int R, T, H, k, E_loc, weighted;
+    int64_t ntok;
+    uint32_t* err;
+};
+
+template <int U>
+__global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
+    __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
+    __shared__ float s_coef[kWarps][EP_MAX_RANKS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+
+    for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
+        int nd = 0;
+        for (int d0 = 0; d0 < a.R; d0 += 32) {
+            const int d = d0 + lane;
+            int64_t row = -1;
+            float coef = 1.0f;
+            if (d < a.R) {
+                const int h = a.send_head[g * a.R + d];
+                if (h >= 0) {
+                    row = a.off.v[d] + h;
+                    if (row >= a.off.v[d + 1]) {
+                        raise_flag(a.err, EP_DEVERR_RECV_OVERFLOW);
+                        row = -1;
+                    }
+                }
+                if (row >= 0 && a.weighted) {
+                    coef = 0.0f;
+                    for (int j = 0; j < a.k; ++j) {
+                        const int64_t e = a.topk_idx[g * a.k + j];
+                        if (e >= 0 && e / a.E_loc == d) coef += a.topk_weights[g * a.k + j];
+                    }
+                }
+            }
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
+            if (row >= 0) {
+                const int p = nd + __popc(bal & lanemask_lt());
+                s_row[warp][p] = row;
+                s_coef[warp][p] = coef;
+            }
+            nd += __popc(bal);
+        }
+        __syncwarp();
+
+        if (a.combined_topk_weights != nullptr && lane < a.k) {
+            float sum = 0.0f;
+            for (int p = 0; p < nd; ++p) sum += a.recv_topk_weights[s_row[warp][p] * a.k + lane];
+            a.combined_topk_weights[g * a.k + lane] = sum;
+        }
+
+        gather_reduce_row<U>(a.y, s_row[warp], s_coef[warp], nd, a.H,
+                             a.out + g * (int64_t)a.H * 2, lane, 32);
+        __syncwarp();
+    }
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" ep_status ep_combine(const ep_shape* sh, const void* y, const int64_t* y_row_offset,
+                                const ep_handle* handle, ep_combine_mode mode,
+                                const int64_t* topk_idx, const float* topk_weights,
+                                const float* recv_topk_weights, void* out,
+                                float* combined_topk_weights, const ep_launch* launch) {
+    using namespace ep;
+    ep_status st = check_shape(sh);
+    if (st != EP_OK) return st;
+    if (handle == nullptr || launch == nullptr) return EP_ERR_INVALID_ARG;
+    const int64_t ntok = (int64_t)sh->num_ranks * sh->num_tokens;
+    if (ntok > 0 && handle->send_head == nullptr) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && (y == nullptr || out == nullptr)) return EP_ERR_INVALID_ARG;
+    if (mode != EP_COMBINE_SUM && mode != EP_COMBINE_WEIGHTED) return EP_ERR_INVALID_ARG;
+    if (mode == EP_COMBINE_WEIGHTED && ntok > 0 && (topk_idx == nullptr || topk_weights == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if ((combined_topk_weights == nullptr) != (recv_topk_weights == nullptr)) return EP_ERR_INVALID_ARG;
+    if (((uintptr_t)y & 15) != 0 || ((uintptr_t)out & 15) != 0) return EP_ERR_INVALID_ARG;
+
+    CombineArgs a{};
+    if ((st = load_row_offsets(y_row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
+    a.y = reinterpret_cast<const char*>(y);
+    a.send_head = handle->send_head;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.recv_topk_weights = recv_topk_weights;
+    a.out = reinterpret_cast<char*>(out);
+    a.combined_topk_weights = combined_topk_weights;
+    a.R = sh->num_ranks;
+    a.T = sh->num_tokens;
+    a.H = sh->hidden;
+    a.k = sh->num_topk;
+    a.E_loc = sh->num_experts / sh->num_ranks;
+    a.weighted = mode == EP_COMBINE_WEIGHTED;
+    a.ntok = ntok;
+    a.err = launch->error_flags;
+
+    if ((st = begin_call(launch)) != EP_OK) return st;
+    if (ntok > 0) {
+        int64_t blocks = (ntok + kWarps - 1) / kWarps;
+        if (sh->num_sms > 0) {
+            int per_sm = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<2>, kThreads, 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+            const int64_t cap = (int64_t)sh->num_sms * (per_sm > 0 ? per_sm : 1);
+            if (blocks > cap) blocks = cap;
+        }
+        combine_kernel<2><<<(unsigned)blocks, kThreads, 0, launch->stream>>>(a);
+        count_launches(1);
+    }
+    return end_call(launch);
+}

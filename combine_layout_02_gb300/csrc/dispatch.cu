@@ -1,0 +1,191 @@
+// dispatch.cu -- normal-mode dispatch: every source token row is read once and
+// stored to each virtual rank it is routed to.
+//
+// [README] "DeepEP" README (EnflameTechnology/DeepEP), normal-kernel example:
+//          dispatch(x, topk_idx, topk_weights, ...) -> recv_x, recv_topk_idx,
+//          recv_topk_weights, num_recv_tokens_per_expert_list, handle; x may be bf16
+//          or a pre-quantised (fp8, scales) tuple; feature notes: FP8 dispatch with
+//          per-group scales; combine_backward = dispatch with the handle.
+// [REUSE]  "How DeepEP Optimizes Handle Reuse for Repeated Dispatches", "Fast Path
+//          Dispatch with Handle Reuse": with a handle, no topk is passed and the
+//          cached layout is used directly.
+//
+// One warp per source token: the warp reads the token's send_head row, compacts the
+// destination rows into shared memory (ballot + popc, ascending rank order), writes
+// the per-row metadata, then streams the payload. In one device memory the
+// all-to-all reduces to this scatter; nothing is exchanged between GPUs.
+#include "rowops.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+enum { kCopy = 0, kQuant = 1 };
+
+struct DispatchArgs {
+    const char* x;
+    const float* x_scales;          // pre-quantised input only
+    const int64_t* topk_idx;        // nullable (handle reuse)
+    const float* topk_weights;      // nullable
+    const int32_t* send_head;
+    char* recv_x;
+    float* recv_x_scales;
+    int64_t* recv_topk_idx;
+    float* recv_topk_weights;
+    int32_t* recv_src_idx;
+    RowOffsets off;
+    int R, T, H, k, E_loc;
+    int in_elem;                    // bytes per element of x
+    int copy_scales;                // pre-quantised input: copy x_scales rows too
+    int64_t ntok;                   // R * T
+    uint32_t* err;
+};
+
+template <int MODE, int U>
+__global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
+    __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
+    __shared__ int s_dst[kWarps][EP_MAX_RANKS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t out_row_bytes = (int64_t)a.H * (MODE == kQuant ? 1 : a.in_elem);
+    const int G = a.H >> 7;
+
+    for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
+        const int t = (int)(g % a.T);
+
+        // Destination rows in ascending rank order.
+        int nd = 0;
+        for (int d0 = 0; d0 < a.R; d0 += 32) {
+            const int d = d0 + lane;
+            int64_t row = -1;
+            if (d < a.R) {
+                const int h = a.send_head[g * a.R + d];
+                if (h >= 0) {
+                    row = a.off.v[d] + h;
+                    if (row >= a.off.v[d + 1]) {
+                        raise_flag(a.err, EP_DEVERR_RECV_OVERFLOW);
+                        row = -1;
+                    }
+                }
+            }
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
+            if (row >= 0) {
+                const int p = nd + __popc(bal & lanemask_lt());
+                s_row[warp][p] = row;
+                s_dst[warp][p] = d;
+            }
+            nd += __popc(bal);
+        }
+        __syncwarp();
+
+        // Per-row metadata.
+        if (a.recv_src_idx != nullptr)
+            for (int p = lane; p < nd; p += 32) a.recv_src_idx[s_row[warp][p]] = t;
+        if (a.topk_idx != nullptr && lane < a.k) {
+            const int64_t e = a.topk_idx[g * a.k + lane];
+            const float wgt = a.topk_weights != nullptr ? a.topk_weights[g * a.k + lane] : 0.0f;
+            for (int p = 0; p < nd; ++p) {
+                const int64_t row = s_row[warp][p];
+                const int d = s_dst[warp][p];
+                const bool local = e >= 0 && e / a.E_loc == d;
+                a.recv_topk_idx[row * a.k + lane] = local ? e - (int64_t)d * a.E_loc : -1;
+                if (a.recv_topk_weights != nullptr)
+                    a.recv_topk_weights[row * a.k + lane] = local ? wgt : 0.0f;
+            }
+        }
+
+        // Payload.
+        const char* src = a.x + g * (int64_t)a.H * a.in_elem;
+        if (MODE == kCopy) {
+            scatter_copy_row<U>(src, a.recv_x, s_row[warp], nd, out_row_bytes, lane, 32);
+            if (a.copy_scales) {
+                const float* ss = a.x_scales + g * G;
+                for (int p = 0; p < nd; ++p)
+                    for (int i = lane; i < G; i += 32) a.recv_x_scales[s_row[warp][p] * G + i] = ss[i];
+            }
+        } else {
+            scatter_quant_row<U>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
+                                 s_row[warp], nd, a.H, lane, 32);
+        }
+        __syncwarp();
+    }
+}
+
+template <int MODE, int U>
+ep_status launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
+    if (a.ntok == 0) return EP_OK;
+    int64_t blocks = (a.ntok + kWarps - 1) / kWarps;
+    if (num_sms > 0) {
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<MODE, U>, kThreads, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const int64_t cap = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > cap) blocks = cap;
+    }
+    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    dispatch_kernel<MODE, U><<<(unsigned)blocks, kThreads, 0, stream>>>(a);
+    count_launches(1);
+    return EP_OK;
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_dtype,
+                                 const float* x_scales, ep_dtype recv_dtype,
+                                 const int64_t* topk_idx, const float* topk_weights,
+                                 const ep_handle* handle, ep_recv* out, const ep_launch* launch) {
+    using namespace ep;
+    ep_status st = check_shape(sh);
+    if (st != EP_OK) return st;
+    if (handle == nullptr || out == nullptr || launch == nullptr) return EP_ERR_INVALID_ARG;
+    const int64_t ntok = (int64_t)sh->num_ranks * sh->num_tokens;
+    if (ntok > 0 && handle->send_head == nullptr) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && (x == nullptr || out->recv_x == nullptr)) return EP_ERR_INVALID_ARG;
+    if (x_dtype == EP_FP8_E4M3 && recv_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (x_dtype != EP_BF16 && x_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (recv_dtype != EP_BF16 && recv_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (recv_dtype == EP_FP8_E4M3 && out->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
+    if (x_dtype == EP_FP8_E4M3 && ntok > 0 && x_scales == nullptr) return EP_ERR_INVALID_ARG;
+    // Handle reuse passes no topk (the pages assert this); topk outputs then cannot be
+    // produced. A first dispatch passes topk_idx and gets recv_topk_idx.
+    if (topk_idx == nullptr && (topk_weights != nullptr || out->recv_topk_idx != nullptr ||
+                                out->recv_topk_weights != nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (topk_idx != nullptr && out->recv_topk_idx == nullptr) return EP_ERR_INVALID_ARG;
+    if (topk_weights == nullptr && out->recv_topk_weights != nullptr) return EP_ERR_INVALID_ARG;
+    // 16-byte vector access of rows.
+    if (((uintptr_t)x & 15) != 0 || ((uintptr_t)out->recv_x & 15) != 0) return EP_ERR_INVALID_ARG;
+
+    DispatchArgs a{};
+    if ((st = load_row_offsets(out->row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
+    a.x = reinterpret_cast<const char*>(x);
+    a.x_scales = x_scales;
+    a.topk_idx = topk_idx;
+    a.topk_weights = topk_weights;
+    a.send_head = handle->send_head;
+    a.recv_x = reinterpret_cast<char*>(out->recv_x);
+    a.recv_x_scales = out->recv_x_scales;
+    a.recv_topk_idx = out->recv_topk_idx;
+    a.recv_topk_weights = out->recv_topk_weights;
+    a.recv_src_idx = out->recv_src_idx;
+    a.R = sh->num_ranks;
+    a.T = sh->num_tokens;
+    a.H = sh->hidden;
+    a.k = sh->num_topk;
+    a.E_loc = sh->num_experts / sh->num_ranks;
+    a.in_elem = x_dtype == EP_BF16 ? 2 : 1;
+    a.copy_scales = x_dtype == EP_FP8_E4M3 ? 1 : 0;
+    a.ntok = ntok;
+    a.err = launch->error_flags;
+
+    if ((st = begin_call(launch)) != EP_OK) return st;
+    if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)
+        st = launch_dispatch<kQuant, 2>(a, sh->num_sms, launch->stream);
+    else
+        st = launch_dispatch<kCopy, 4>(a, sh->num_sms, launch->stream);
+    if (st != EP_OK) return st;
+    return end_call(launch);
+}

@@ -1,0 +1,103 @@
+// ep_internal.cuh -- helpers shared by the libep translation units (device memory
+// access with cache hints, bf16 / e4m3 packing, host-side validation, event
+// ordering and launch accounting). Internal: not part of the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ep.h"
+
+namespace ep {
+
+// ------------------------------------------------------------------ device helpers
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    // Read-only, streaming: each source byte is read once, keep it out of L1.
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, const uint4& v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_stream_v4(void* p, const uint4& v) {
+    // Streaming store (evict-first): the written rows are far larger than L2.
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+                 "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// bf16 pair packed in a 32-bit word -> two fp32 (exact widening: bf16 is the high
+// half of a binary32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16 pair, round to nearest even (CUDA's documented conversion).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two fp32 -> packed e4m3 pair (lo in the low byte), round to nearest even,
+// saturating to +-448 (CUDA's documented fp8 conversion, __NV_SATFINITE).
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+    __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+    return static_cast<uint32_t>(s);
+}
+
+__device__ __forceinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
+    if (flags != nullptr) atomicOr(flags, bit);
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Destination-row regions passed by value (host array copied into kernel params).
+struct RowOffsets {
+    int64_t v[EP_MAX_RANKS + 1];
+};
+
+// ------------------------------------------------------------------ host helpers
+
+// Validates the shape (limits stated in ep.h). Returns EP_OK or an error status.
+ep_status check_shape(const ep_shape* sh);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Makes launch->stream wait on launch->wait_event (if any).
+ep_status begin_call(const ep_launch* launch);
+
+// Checks the launch error state, then records launch->record_event (if any).
+ep_status end_call(const ep_launch* launch);
+
+// Records a CUDA error for ep_last_cuda_error and returns EP_ERR_CUDA.
+ep_status cuda_fail(cudaError_t e);
+
+// Adds n to the process-wide kernel launch counter.
+void count_launches(uint64_t n);
+
+// Fills a RowOffsets from a host array of R+1 entries; checks monotonicity.
+ep_status load_row_offsets(const int64_t* host, int R, RowOffsets* out);
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace ep

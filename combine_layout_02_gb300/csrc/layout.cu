@@ -1,0 +1,276 @@
+// layout.cu -- get_dispatch_layout and the handle's prefix matrices on the device.
+//
+// [README]  "DeepEP" README (EnflameTechnology/DeepEP), normal-kernel example:
+//           get_dispatch_layout(topk_idx, num_experts, ...) -> num_tokens_per_rank,
+//           num_tokens_per_rdma_rank, num_tokens_per_expert, is_token_in_rank.
+// [REUSE]   "How DeepEP Optimizes Handle Reuse for Repeated Dispatches", "What the
+//           Handle Contains": rank_prefix_matrix, channel_prefix_matrix,
+//           recv_channel_prefix_matrix, recv_src_idx, is_token_in_rank, send_head.
+//
+// Two kernels, one block per (channel c, source rank s); no atomics on global memory,
+// no inter-block waiting, so every result is deterministic:
+//   layout_count_kernel  -- per block: expert histogram (shared-memory atomics),
+//       is_token_in_rank bytes, per-destination counts of the channel (warp ballot +
+//       popc). Partial counts go to the caller's workspace.
+//   layout_prefix_kernel -- per block: the prefix entries of its (s, c) from the
+//       partial counts (warp reductions), the expert totals, and send_head for its
+//       tokens by a block-wide exclusive scan of the rank bits (ballot + popc within a
+//       warp, shared-memory scan across warps).
+// Rows of destination d are ordered by (source rank, token), so
+//   send_head[s][t][d] = recv_channel_prefix_matrix[d][s][c(t)]
+//                        + #{t' < t in the same channel with is_token_in_rank}.
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct LayoutArgs {
+    const int64_t* topk_idx;
+    int R, T, E, k, C, E_loc, tpc;
+    int32_t* num_tokens_per_rank;         // [R][R] nullable
+    int32_t* num_tokens_per_expert;       // [R][E] nullable
+    uint8_t* in_rank;                     // [R][T][R] (handle)
+    uint8_t* in_rank_extra;               // [R][T][R] nullable second copy (layout)
+    int32_t* rank_prefix;                 // [R][R]
+    int32_t* channel_prefix;              // [R][R][C]
+    int32_t* recv_channel_prefix;         // [R][R][C]
+    int32_t* send_head;                   // [R][T][R]
+    int32_t* num_recv_per_expert;         // [R][E_loc] == [E]
+    int32_t* ws_cnt;                      // [R][R][C]: (s*R + d)*C + c
+    int32_t* ws_expert;                   // [R][C][E]: (s*C + c)*E + e
+    uint32_t* err;
+};
+
+__device__ __forceinline__ void write_rank_bytes(uint8_t* p, uint64_t mask, int R) {
+    if ((R & 7) == 0) {
+        for (int d8 = 0; d8 < R; d8 += 8) {
+            uint64_t w = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) w |= ((mask >> (d8 + i)) & 1ull) << (8 * i);
+            *reinterpret_cast<uint64_t*>(p + d8) = w;
+        }
+    } else {
+        for (int d = 0; d < R; ++d) p[d] = (uint8_t)((mask >> d) & 1ull);
+    }
+}
+
+__device__ __forceinline__ uint64_t read_rank_bytes(const uint8_t* p, int R) {
+    uint64_t mask = 0;
+    if ((R & 7) == 0) {
+        for (int d8 = 0; d8 < R; d8 += 8) {
+            uint64_t w = *reinterpret_cast<const uint64_t*>(p + d8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mask |= ((w >> (8 * i)) & 1ull) << (d8 + i);
+        }
+    } else {
+        for (int d = 0; d < R; ++d) mask |= (uint64_t)(p[d] & 1) << d;
+    }
+    return mask;
+}
+
+__global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
+    extern __shared__ int smem[];
+    int* hist = smem;          // [E]
+    int* cnt = smem + a.E;     // [R]
+    const int c = blockIdx.x, s = blockIdx.y, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < a.E; i += kThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i < a.R; i += kThreads) cnt[i] = 0;
+    __syncthreads();
+
+    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
+    for (int base = t0; base < t1; base += kThreads) {   // block-uniform trip count
+        const int t = base + threadIdx.x;
+        uint64_t mask = 0;
+        if (t < t1) {
+            const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t) * a.k;
+            for (int j = 0; j < a.k; ++j) {
+                const int64_t e = row[j];
+                if (e == -1) continue;
+                if (e < 0 || e >= a.E) {
+                    raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
+                    continue;
+                }
+                atomicAdd(&hist[(int)e], 1);
+                mask |= 1ull << ((int)e / a.E_loc);
+            }
+            const int64_t off = ((int64_t)s * a.T + t) * a.R;
+            write_rank_bytes(a.in_rank + off, mask, a.R);
+            if (a.in_rank_extra != nullptr) write_rank_bytes(a.in_rank_extra + off, mask, a.R);
+        }
+        for (int d = 0; d < a.R; ++d) {
+            const unsigned b = __ballot_sync(0xFFFFFFFFu, (mask >> d) & 1ull);
+            if (lane == 0 && b != 0) atomicAdd(&cnt[d], __popc(b));
+        }
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < a.R; d += kThreads)
+        a.ws_cnt[((int64_t)s * a.R + d) * a.C + c] = cnt[d];
+    int32_t* we = a.ws_expert + ((int64_t)s * a.C + c) * a.E;
+    for (int e = threadIdx.x; e < a.E; e += kThreads) we[e] = hist[e];
+}
+
+__global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
+    __shared__ int s_base[EP_MAX_RANKS];
+    __shared__ int s_warp_tot[kWarps][EP_MAX_RANKS];
+    __shared__ int s_warp_off[kWarps][EP_MAX_RANKS];
+    const int c = blockIdx.x, s = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int R = a.R, C = a.C, E = a.E;
+
+    // (1) One warp per destination d: A = tokens of earlier sources, B = tokens of
+    // earlier channels of s, own = this channel, F = all channels of s.
+    for (int d = warp; d < R; d += kWarps) {
+        int A = 0, B = 0, own = 0, F = 0;
+        for (int i = lane; i < s * C; i += 32) {
+            const int sp = i / C, cp = i - sp * C;
+            A += a.ws_cnt[((int64_t)sp * R + d) * C + cp];
+        }
+        for (int cp = lane; cp < C; cp += 32) {
+            const int v = a.ws_cnt[((int64_t)s * R + d) * C + cp];
+            F += v;
+            if (cp < c) B += v;
+            if (cp == c) own = v;
+        }
+        A = warp_sum(A);
+        B = warp_sum(B);
+        own = warp_sum(own);
+        F = warp_sum(F);
+        if (lane == 0) {
+            s_base[d] = A + B;
+            a.recv_channel_prefix[((int64_t)d * R + s) * C + c] = A + B;
+            a.channel_prefix[((int64_t)s * R + d) * C + c] = B + own;
+            if (c == 0) {
+                a.rank_prefix[s * R + d] = A + F;
+                if (a.num_tokens_per_rank != nullptr) a.num_tokens_per_rank[s * R + d] = F;
+            }
+        }
+    }
+
+    // (2) Expert totals, spread over every block of the grid.
+    const int nblocks = R * C, b = s * C + c;
+    if (a.num_tokens_per_expert != nullptr) {
+        for (int p = b * kThreads + threadIdx.x; p < R * E; p += nblocks * kThreads) {
+            const int sp = p / E, e = p - sp * E;
+            int sum = 0;
+            for (int cp = 0; cp < C; ++cp) sum += a.ws_expert[((int64_t)sp * C + cp) * E + e];
+            a.num_tokens_per_expert[p] = sum;
+        }
+    }
+    for (int e = b * kWarps + warp; e < E; e += nblocks * kWarps) {
+        int sum = 0;
+        for (int i = lane; i < R * C; i += 32) sum += a.ws_expert[(int64_t)i * E + e];
+        sum = warp_sum(sum);
+        if (lane == 0) a.num_recv_per_expert[e] = sum;
+    }
+    __syncthreads();
+
+    // (3) send_head for the tokens of channel c of source s.
+    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
+    for (int tile = t0; tile < t1; tile += kThreads) {   // block-uniform trip count
+        const int t = tile + threadIdx.x;
+        const uint64_t mask = (t < t1) ? read_rank_bytes(a.in_rank + ((int64_t)s * a.T + t) * R, R) : 0ull;
+        for (int d = 0; d < R; ++d) {
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, (mask >> d) & 1ull);
+            if (lane == 0) s_warp_tot[warp][d] = __popc(bal);
+        }
+        __syncthreads();
+        if (threadIdx.x < R) {
+            const int d = threadIdx.x;
+            int run = s_base[d];
+            for (int w = 0; w < kWarps; ++w) {
+                s_warp_off[w][d] = run;
+                run += s_warp_tot[w][d];
+            }
+            s_base[d] = run;
+        }
+        __syncthreads();
+        const uint32_t lt = lanemask_lt();
+        int32_t* out = a.send_head + ((int64_t)s * a.T + t) * R;
+        for (int d = 0; d < R; ++d) {
+            const bool in = (mask >> d) & 1ull;
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+            if (t < t1) out[d] = in ? s_warp_off[warp][d] + __popc(bal & lt) : -1;
+        }
+        __syncthreads();
+    }
+}
+
+size_t ws_cnt_bytes(const ep_shape* sh) {
+    const size_t n = (size_t)sh->num_ranks * sh->num_ranks * sh->num_channels * sizeof(int32_t);
+    return (n + 255) & ~(size_t)255;
+}
+
+}  // namespace
+}  // namespace ep
+
+extern "C" {
+
+size_t ep_layout_workspace_size(const ep_shape* sh) {
+    if (ep::check_shape(sh) != EP_OK) return 0;
+    return ep::ws_cnt_bytes(sh) +
+           (size_t)sh->num_ranks * sh->num_channels * sh->num_experts * sizeof(int32_t);
+}
+
+ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* layout,
+                        ep_handle* handle, void* workspace, size_t workspace_bytes,
+                        const ep_launch* launch) {
+    using namespace ep;
+    ep_status st = check_shape(sh);
+    if (st != EP_OK) return st;
+    if (handle == nullptr || launch == nullptr) return EP_ERR_INVALID_ARG;
+    if (handle->rank_prefix_matrix == nullptr || handle->channel_prefix_matrix == nullptr ||
+        handle->recv_channel_prefix_matrix == nullptr || handle->num_recv_tokens_per_expert == nullptr)
+        return EP_ERR_INVALID_ARG;
+    // Per-token arrays are empty (and may be NULL) when there are no tokens.
+    if (sh->num_tokens > 0 && (handle->is_token_in_rank == nullptr || handle->send_head == nullptr))
+        return EP_ERR_INVALID_ARG;
+    if (layout != nullptr && layout->num_tokens_per_rdma_rank != nullptr) return EP_ERR_INVALID_ARG;
+    if (sh->num_tokens > 0 && topk_idx == nullptr) return EP_ERR_INVALID_ARG;
+    const size_t need = ep_layout_workspace_size(sh);
+    if (workspace == nullptr || workspace_bytes < need || ((uintptr_t)workspace & 15) != 0)
+        return EP_ERR_INVALID_ARG;
+    if ((sh->num_ranks & 7) == 0) {
+        // 8-byte vector access of is_token_in_rank rows needs 8-byte alignment.
+        if (((uintptr_t)handle->is_token_in_rank & 7) != 0) return EP_ERR_INVALID_ARG;
+        if (layout != nullptr && layout->is_token_in_rank != nullptr &&
+            ((uintptr_t)layout->is_token_in_rank & 7) != 0)
+            return EP_ERR_INVALID_ARG;
+    }
+
+    LayoutArgs a{};
+    a.topk_idx = topk_idx;
+    a.R = sh->num_ranks;
+    a.T = sh->num_tokens;
+    a.E = sh->num_experts;
+    a.k = sh->num_topk;
+    a.C = sh->num_channels;
+    a.E_loc = a.E / a.R;
+    a.tpc = a.T > 0 ? ceil_div(a.T, a.C) : 1;
+    a.num_tokens_per_rank = layout ? layout->num_tokens_per_rank : nullptr;
+    a.num_tokens_per_expert = layout ? layout->num_tokens_per_expert : nullptr;
+    a.in_rank = handle->is_token_in_rank;
+    a.in_rank_extra = (layout && layout->is_token_in_rank != handle->is_token_in_rank)
+                          ? layout->is_token_in_rank
+                          : nullptr;
+    a.rank_prefix = handle->rank_prefix_matrix;
+    a.channel_prefix = handle->channel_prefix_matrix;
+    a.recv_channel_prefix = handle->recv_channel_prefix_matrix;
+    a.send_head = handle->send_head;
+    a.num_recv_per_expert = handle->num_recv_tokens_per_expert;
+    a.ws_cnt = reinterpret_cast<int32_t*>(workspace);
+    a.ws_expert = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + ws_cnt_bytes(sh));
+    a.err = launch->error_flags;
+
+    if ((st = begin_call(launch)) != EP_OK) return st;
+    const dim3 grid(a.C, a.R);
+    const size_t smem = sizeof(int) * (size_t)(a.E + a.R);
+    layout_count_kernel<<<grid, kThreads, smem, launch->stream>>>(a);
+    layout_prefix_kernel<<<grid, kThreads, 0, launch->stream>>>(a);
+    count_launches(2);
+    return end_call(launch);
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+// rowops.cuh -- the three row movements of the hot path, written once and used by
+// both the normal (one warp per token) and the low-latency (one block per token)
+// kernels:
+//   scatter_copy_row   one source row -> nd destination rows (bytes copied)
+//   scatter_quant_row  one bf16 source row -> e4m3 row + per-128-channel fp32 scales,
+//                      quantised once, stored to nd destination rows
+//   gather_reduce_row  nd bf16 rows * coefficients -> one bf16 row, fp32 accumulation
+// Work is split in 16-byte units: thread `first` handles units first, first+stride, ...
+// Each source byte is loaded once (ld.global.nc, no L1 allocation) and every
+// destination byte stored once with 16-byte vector stores; loads of an unrolled batch
+// are all issued before their data is used, to keep enough bytes in flight.
+#pragma once
+
+#include "ep_internal.cuh"
+
+namespace ep {
+
+template <int U>
+__device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
+                                                 char* __restrict__ dst_base,
+                                                 const int64_t* rows, int nd, int64_t row_bytes,
+                                                 int first, int stride) {
+    const int units = (int)(row_bytes >> 4);
+    for (int u0 = 0; u0 < units; u0 += stride * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int u = u0 + i * stride + first;
+            if (u < units) v[i] = ld_stream_v4(src + (int64_t)u * 16);
+        }
+        for (int p = 0; p < nd; ++p) {
+            char* dst = dst_base + rows[p] * row_bytes;
+#pragma unroll
+            for (int i = 0; i < U; ++i) {
+                const int u = u0 + i * stride + first;
+                if (u < units) st_v4(dst + (int64_t)u * 16, v[i]);
+            }
+        }
+    }
+}
+
+// FP8 e4m3 quantisation, one scale per 128 channels ("DeepEP" README feature notes:
+// FP8 dispatch with per-group scales). Unit = 16 channels (32 bytes of bf16 in, 16
+// bytes of e4m3 out); 8 consecutive units (8 consecutive lanes) form one group, so the
+// group amax is a 3-step xor-shuffle. `stride` must be a multiple of 32 and `first`
+// the thread's index in a block or warp whose size is `stride`; every lane of a warp
+// must call this (the shuffles use the full mask).
+//   amax' = max(amax, 1e-4), scale = amax' / 448 (IEEE division),
+//   inv = 448 / amax' (IEEE division), q = e4m3_rn_satfinite(x * inv).
+template <int U>
+__device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
+                                                  uint8_t* __restrict__ q_base,
+                                                  float* __restrict__ s_base,
+                                                  const int64_t* rows, int nd, int H,
+                                                  int first, int stride) {
+    const int units = H >> 4;
+    const int G = H >> 7;
+    for (int u0 = 0; u0 < units; u0 += stride * U) {
+        uint4 a[U], b[U];
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int u = u0 + i * stride + first;
+            if (u < units) {
+                a[i] = ld_stream_v4(src + (int64_t)u * 32);
+                b[i] = ld_stream_v4(src + (int64_t)u * 32 + 16);
+            } else {
+                a[i] = make_uint4(0, 0, 0, 0);
+                b[i] = make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int u = u0 + i * stride + first;
+            const uint32_t w[8] = {a[i].x, a[i].y, a[i].z, a[i].w, b[i].x, b[i].y, b[i].z, b[i].w};
+            float f[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                f[2 * j] = bf16_lo(w[j]);
+                f[2 * j + 1] = bf16_hi(w[j]);
+            }
+            float amax = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+            const float am = fmaxf(amax, 1e-4f);
+            const float scale = __fdiv_rn(am, 448.0f);
+            const float inv = __fdiv_rn(448.0f, am);
+            uint4 q;
+            uint32_t qw[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
+                const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
+                qw[j] = lo | (hi << 16);
+            }
+            q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+            if (u < units) {
+                for (int p = 0; p < nd; ++p) {
+                    st_v4(q_base + rows[p] * (int64_t)H + (int64_t)u * 16, q);
+                    if ((u & 7) == 0) s_base[rows[p] * (int64_t)G + (u >> 3)] = scale;
+                }
+            }
+        }
+    }
+}
+
+// out = sum_p coef[p] * rows[p], fp32 accumulation in registers, one bf16 RNE store.
+// Unit = 8 channels (16 bytes). Rows are taken 8 at a time with every load of the
+// batch issued before the first accumulation.
+template <int U>
+__device__ __forceinline__ void gather_reduce_row(const char* __restrict__ y_base,
+                                                  const int64_t* rows, const float* coef,
+                                                  int nd, int H, char* __restrict__ out_row,
+                                                  int first, int stride) {
+    constexpr int P = 8;
+    const int units = H >> 3;
+    const int64_t row_bytes = (int64_t)H * 2;
+    for (int u0 = 0; u0 < units; u0 += stride * U) {
+        float acc[U][8];
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int p0 = 0; p0 < nd; p0 += P) {
+            uint4 v[P][U];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (p0 + p < nd) {
+                    const char* src = y_base + rows[p0 + p] * row_bytes;
+#pragma unroll
+                    for (int i = 0; i < U; ++i) {
+                        const int u = u0 + i * stride + first;
+                        if (u < units) v[p][i] = ld_stream_v4(src + (int64_t)u * 16);
+                    }
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (p0 + p < nd) {
+                    const float c = coef[p0 + p];
+#pragma unroll
+                    for (int i = 0; i < U; ++i) {
+                        const uint32_t w[4] = {v[p][i].x, v[p][i].y, v[p][i].z, v[p][i].w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            acc[i][2 * j] = fmaf(c, bf16_lo(w[j]), acc[i][2 * j]);
+                            acc[i][2 * j + 1] = fmaf(c, bf16_hi(w[j]), acc[i][2 * j + 1]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int u = u0 + i * stride + first;
+            if (u < units) {
+                const uint4 o = make_uint4(pack_bf16x2(acc[i][0], acc[i][1]), pack_bf16x2(acc[i][2], acc[i][3]),
+                                           pack_bf16x2(acc[i][4], acc[i][5]), pack_bf16x2(acc[i][6], acc[i][7]));
+                st_v4(out_row + (int64_t)u * 16, o);
+            }
+        }
+    }
+}
+
+}  // namespace ep

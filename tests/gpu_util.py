@@ -1,0 +1,91 @@
+"""Helpers for the GPU parity tests: move seeded numpy inputs to the device, run the
+C-ABI path, bring results back as numpy arrays in the oracle's conventions (bf16 as
+uint16 bit patterns, e4m3 as uint8)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import combine_layout_02_gb300 as ep
+from combine_layout_02_gb300.buffers import LayoutBuffers, LLBuffers, RecvBuffers
+
+ATOL, RTOL = 1e-3, 1e-2          # combine tolerance (bf16 output, fp32 accumulation)
+
+
+def dev_bf16(x_bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(x_bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def host_bits(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint32) << 16).astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def assert_close_bf16(got_bits, exp_bits, atol=ATOL, rtol=RTOL):
+    g, e = bf16_to_f64(got_bits), bf16_to_f64(exp_bits)
+    bad = np.abs(g - e) > atol + rtol * np.abs(e)
+    assert not bad.any(), f"{bad.sum()} elements outside tolerance; first at {np.argwhere(bad)[0]}"
+
+
+def compact_offsets(rank_prefix: np.ndarray) -> list:
+    off = [0]
+    for n in rank_prefix[-1]:
+        off.append(off[-1] + int(n))
+    return off
+
+
+class GpuRun:
+    """Holds device inputs and buffers of one workload."""
+
+    def __init__(self, R, T, H, E, k, C, inp, nmax=0):
+        self.R, self.T, self.H, self.E, self.k, self.C = R, T, H, E, k, C
+        self.sh = ep.make_shape(R, T, H, E, k, C, nmax=nmax)
+        self.inp = inp
+        self.topk = torch.from_numpy(inp["topk_idx"]).cuda()
+        self.wts = torch.from_numpy(inp["topk_weights"]).cuda()
+        self.x = dev_bf16(inp["x"]) if inp.get("x") is not None else None
+        self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        self.launch = ep.make_launch(error_flags=self.err)
+        self.lb = None
+
+    def flags(self) -> int:
+        torch.cuda.synchronize()
+        return int(self.err.item())
+
+    def layout(self) -> dict:
+        self.lb = LayoutBuffers(self.sh)
+        ep.ep_get_layout(self.sh, self.topk, self.lb.layout(), self.lb.handle(), self.lb.workspace,
+                         self.launch)
+        return {k: v.cpu().numpy() for k, v in self.lb.as_dict().items()}
+
+    def dispatch(self, off, recv_dtype=ep.EP_BF16, with_topk=True, x=None, x_dtype=ep.EP_BF16,
+                 x_scales=None, fill=0xA5) -> RecvBuffers:
+        rb = RecvBuffers(off[-1], self.H, self.k, recv_dtype=recv_dtype, with_topk=with_topk, fill=fill)
+        ep.ep_dispatch(self.sh, self.x if x is None else x, x_dtype, x_scales, recv_dtype,
+                       self.topk if with_topk else None, self.wts if with_topk else None,
+                       self.lb.handle(rb.recv_src_idx), rb.recv_x, rb.recv_x_scales,
+                       rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx, off, self.launch)
+        return rb
+
+    def combine(self, y: torch.Tensor, off, mode, recv_topk_weights=None) -> tuple:
+        out = torch.empty((self.R, self.T, self.H), dtype=torch.bfloat16, device="cuda")
+        cw = (torch.empty((self.R, self.T, self.k), dtype=torch.float32, device="cuda")
+              if recv_topk_weights is not None else None)
+        ep.ep_combine(self.sh, y, off, self.lb.handle(), mode, self.topk, self.wts,
+                      recv_topk_weights, out, cw, self.launch)
+        return out, cw
+
+    def ll_dispatch(self, use_fp8: bool, phase=ep.EP_PHASE_BOTH, buf: LLBuffers = None) -> LLBuffers:
+        buf = buf or LLBuffers(self.sh, use_fp8, fill=0x5A)
+        ep.ep_ll_dispatch(self.sh, self.x, self.topk, use_fp8, phase, buf.struct(), self.launch)
+        return buf
+
+    def ll_combine(self, y: torch.Tensor, buf: LLBuffers, phase=ep.EP_PHASE_BOTH) -> torch.Tensor:
+        out = torch.empty((self.R, self.T, self.H), dtype=torch.bfloat16, device="cuda")
+        ep.ep_ll_combine(self.sh, y, self.topk, self.wts, buf.struct(), phase, out, self.launch)
+        return out

@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every symbol include/ep.h declares;
+host-side argument validation rejects bad calls before any CUDA work (no GPU needed:
+no call here reaches a kernel launch or a CUDA API)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ep():
+    from combine_layout_02_gb300 import build
+    build.build()
+    import combine_layout_02_gb300 as ep
+    ep.lib()
+    return ep
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ep.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set()
+    for m in re.finditer(r"^[A-Za-z_][\w \t\*]*?\b(ep_\w+)\s*\(", text, flags=re.M):
+        if not m.group(0).lstrip().startswith(("typedef", "#")):
+            names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(ep):
+    declared = declared_functions()
+    assert declared, "no declarations parsed"
+    assert declared == set(ep.EXPORTED_SYMBOLS)
+    L = ctypes.CDLL(ep.library_path())
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_host_only_helpers(ep):
+    assert ep.ep_abi_version() == 100
+    assert ep.ep_kernel_launch_count() >= 0
+    assert ep.lib().ep_status_string(1).startswith(b"EP_ERR_INVALID_ARG")
+    assert ep.lib().ep_last_cuda_error() == b""
+
+
+def test_workspace_size_formula_and_limits(ep):
+    sh = ep.make_shape(8, 4096, 7168, 256, 8, C=12)
+    ws = ep.ep_layout_workspace_size(sh)
+    cnt = (8 * 8 * 12 * 4 + 255) // 256 * 256
+    assert ws == cnt + 8 * 12 * 256 * 4
+    assert ep.ep_layout_workspace_size(ep.make_shape(65, 16, 128, 65, 1)) == 0     # R > 64
+    assert ep.ep_layout_workspace_size(ep.make_shape(8, 16, 100, 64, 2)) == 0      # H % 128
+    assert ep.ep_layout_workspace_size(ep.make_shape(3, 16, 128, 8, 2)) == 0       # E % R
+
+
+def test_invalid_arguments_rejected_on_host(ep):
+    L = ep.lib()
+    sh = ep.make_shape(2, 4, 128, 4, 2, C=2)
+    launch = ep.ep_launch(None, None, None, None)
+    h = ep.ep_handle()
+    # NULL handle fields
+    st = L.ep_get_layout(ctypes.byref(sh), None, None, ctypes.byref(h), None, 0, ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # dispatch with topk weights but no topk_idx (the handle-reuse assertion)
+    h.send_head = 0x1000
+    out = ep.ep_recv(0x2000, None, None, None, None, None)
+    st = L.ep_dispatch(ctypes.byref(sh), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, 0x4000,
+                       ctypes.byref(h), ctypes.byref(out), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # fp8 input cannot be dispatched as bf16
+    st = L.ep_dispatch(ctypes.byref(sh), 0x3000, ep.EP_FP8_E4M3, 0x5000, ep.EP_BF16, None, None,
+                       ctypes.byref(h), ctypes.byref(out), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # decreasing row offsets
+    off = (ctypes.c_int64 * 3)(0, 10, 5)
+    out.row_offset = ctypes.cast(off, ctypes.c_void_p)
+    st = L.ep_dispatch(ctypes.byref(sh), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,
+                       ctypes.byref(h), ctypes.byref(out), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # weighted combine without weights
+    off2 = (ctypes.c_int64 * 3)(0, 8, 16)
+    st = L.ep_combine(ctypes.byref(sh), 0x3000, ctypes.cast(off2, ctypes.c_void_p), ctypes.byref(h),
+                      ep.EP_COMBINE_WEIGHTED, None, None, None, 0x6000, None, ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # low-latency: T > Nmax
+    sh_ll = ep.make_shape(2, 8, 128, 4, 2, nmax=4)
+    buf = ep.ep_ll_buffer(0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000)
+    st = L.ep_ll_dispatch(ctypes.byref(sh_ll), 0x7000, 0x8000, 0, ep.EP_PHASE_BOTH, ctypes.byref(buf),
+                          ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # bad phase value
+    sh_ll2 = ep.make_shape(2, 4, 128, 4, 2, nmax=4)
+    st = L.ep_ll_dispatch(ctypes.byref(sh_ll2), 0x7000, 0x8000, 0, 4, ctypes.byref(buf),
+                          ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    # unsupported shape
+    big = ep.make_shape(65, 4, 128, 65, 1)
+    st = L.ep_dispatch(ctypes.byref(big), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,
+                       ctypes.byref(h), ctypes.byref(out), ctypes.byref(launch))
+    assert st == ep.EP_ERR_UNSUPPORTED

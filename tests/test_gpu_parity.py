@@ -1,0 +1,290 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by
+element, on seeded inputs spanning several tiles and ragged tails: the tiny workload,
+ragged shapes, R not a multiple of 8, R > 32, R = 1, R = 64, k = 32, empty inputs,
+masked entries, skewed and group-limited routing.
+
+Bit-exact: every layout / handle tensor, receive rows (bf16 and e4m3), FP8 scales,
+recv_topk_idx / recv_topk_weights / recv_src_idx, low-latency slots and counts, and
+the canaries of rows nothing maps to. Combine: within 1e-3 absolute + 1e-2 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import combine_layout_02_gb300 as ep
+import oracle
+import workloads
+from gpu_util import GpuRun, assert_close_bf16, bf16_to_f64, compact_offsets, dev_bf16, host_bits
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.Workload
+CASES = {
+    "tiny": workloads.CONFIGS["tiny"],
+    "ragged": W("ragged", R=4, T=1000, H=384, E=32, k=5, C=7, mask_p=0.1, seed=101),
+    "r3_odd": W("r3", R=3, T=257, H=128, E=9, k=3, C=12, seed=102),
+    "zipf16": W("z16", R=16, T=300, H=512, E=128, k=6, C=5, routing="zipf", zipf_s=1.2, seed=103),
+    "group8": W("g8", R=8, T=513, H=1024, E=256, k=8, C=12, routing="group", groups=8,
+                topk_groups=4, seed=104),
+    "r1": W("r1", R=1, T=70, H=128, E=4, k=2, C=3, seed=105),
+    "r64": W("r64", R=64, T=40, H=128, E=64, k=4, C=2, seed=106),
+    "r33": W("r33", R=33, T=50, H=256, E=66, k=3, C=4, seed=107),
+    "k32": W("k32", R=8, T=64, H=128, E=64, k=32, C=3, seed=108),
+    "many_channels": W("mc", R=2, T=9, H=128, E=8, k=2, C=12, seed=109),
+}
+
+
+def _setup(name):
+    w = CASES[name]
+    inp = workloads.make_workload(w)
+    run = GpuRun(w.R, w.T, w.H, w.E, w.k, w.C, inp)
+    ref = oracle.layout(inp["topk_idx"], w.E, w.C)
+    return w, inp, run, ref
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layout_bit_exact(name):
+    w, inp, run, ref = _setup(name)
+    got = run.layout()
+    for key, arr in got.items():
+        np.testing.assert_array_equal(arr, ref[key], err_msg=key)
+    assert run.flags() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("offsets", ["compact", "worst"])
+def test_dispatch_bf16_bit_exact(name, offsets):
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"]) if offsets == "compact" else \
+        [int(v) for v in workloads.worst_case_row_offsets(w.R, w.T)]
+    rb = run.dispatch(off)
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, inp["topk_idx"],
+                          inp["topk_weights"], fill_x=0xA5A5, fill_idx=-99, fill_w=-5.0, fill_src=-3)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb.recv_src_idx), exp["recv_src_idx"])
+    np.testing.assert_array_equal(host_bits(rb.recv_topk_idx), exp["recv_topk_idx"])
+    np.testing.assert_array_equal(host_bits(rb.recv_topk_weights).view(np.uint32),
+                                  exp["recv_topk_weights"].view(np.uint32))
+    assert run.flags() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r3_odd", "group8", "r33", "k32"])
+def test_dispatch_fp8_fused_bit_exact(name):
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3)
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, inp["topk_idx"],
+                          inp["topk_weights"], x_kind=oracle.X_QUANTIZE)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb.recv_x_scales).view(np.uint32),
+                                  exp["recv_x_scales"].view(np.uint32))
+    np.testing.assert_array_equal(host_bits(rb.recv_topk_idx), exp["recv_topk_idx"])
+    # pre-quantised (fp8, scales) input tuple is copied byte for byte
+    q, sc = oracle.quantize_rows(inp["x"])
+    rb2 = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, with_topk=False,
+                       x=torch.from_numpy(q).cuda(), x_dtype=ep.EP_FP8_E4M3,
+                       x_scales=torch.from_numpy(sc).cuda())
+    np.testing.assert_array_equal(host_bits(rb2.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb2.recv_x_scales).view(np.uint32),
+                                  exp["recv_x_scales"].view(np.uint32))
+    assert run.flags() == 0
+
+
+def test_fp8_extreme_values():
+    """Groups with zeros, values below the amax floor, huge magnitudes, ties."""
+    R, T, H, E, k = 2, 8, 256, 4, 2
+    rng = np.random.default_rng(110)
+    x32 = rng.standard_normal((R, T, H)).astype(np.float32)
+    x32[0, 0] = 0.0
+    x32[0, 1, :128] = 3e-5
+    x32[0, 2] *= 1e30
+    x32[0, 3, 128:] = -1e-38
+    x32[1, 0, :] = np.tile(np.array([2.0, -3 / 1024, 1.0, 0.01], np.float32), H // 4)
+    xb = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    topk = np.tile(np.array([0, 3], np.int64), (R, T, 1))
+    inp = {"x": xb, "topk_idx": topk, "topk_weights": np.full((R, T, k), 0.5, np.float32)}
+    run = GpuRun(R, T, H, E, k, 1, inp)
+    ref = oracle.layout(topk, E, 1)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3)
+    exp = oracle.dispatch(xb, ref["send_head"], np.array(off), E, x_kind=oracle.X_QUANTIZE)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb.recv_x_scales).view(np.uint32),
+                                  exp["recv_x_scales"].view(np.uint32))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_handle_reuse_bit_identical(name):
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    first = run.dispatch(off)
+    again = run.dispatch(off, with_topk=False)
+    assert torch.equal(first.recv_x.view(torch.int16), again.recv_x.view(torch.int16))
+    assert torch.equal(first.recv_src_idx, again.recv_src_idx)
+    # fresh x through the cached handle equals the oracle on that x
+    rng = np.random.default_rng(w.seed + 1000)
+    x2 = workloads.make_hidden(rng, w.R, w.T, w.H)
+    rb = run.dispatch(off, with_topk=False, x=dev_bf16(x2))
+    exp = oracle.dispatch(x2, ref["send_head"], np.array(off), w.E)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("mode", [ep.EP_COMBINE_SUM, ep.EP_COMBINE_WEIGHTED])
+def test_combine_within_tolerance(name, mode):
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rng = np.random.default_rng(w.seed + 2000)
+    y32 = rng.standard_normal((max(off[-1], 1), w.H)).astype(np.float32)
+    yb = torch.from_numpy(y32).to(torch.bfloat16)
+    ybits = yb.view(torch.int16).numpy().view(np.uint16)[: off[-1]]
+    rtw = rng.standard_normal((max(off[-1], 1), w.k)).astype(np.float32)
+    out, cw = run.combine(yb.cuda(), off, mode, recv_topk_weights=torch.from_numpy(rtw).cuda())
+    exp = oracle.combine(ybits, ref["send_head"], np.array(off), w.E, w.k, mode,
+                         inp["topk_idx"], inp["topk_weights"], recv_topk_weights=rtw[: off[-1]])
+    assert_close_bf16(host_bits(out), exp["out"])
+    np.testing.assert_allclose(cw.cpu().numpy(), exp["combined_topk_weights"], rtol=1e-5, atol=1e-6)
+    assert run.flags() == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "zipf16", "group8", "k32"])
+def test_identity_round_trip(name):
+    """dispatch -> identity experts -> weighted combine returns x within bf16 rounding."""
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off)
+    out, _ = run.combine(rb.recv_x, off, ep.EP_COMBINE_WEIGHTED)
+    xf, of = bf16_to_f64(inp["x"]), bf16_to_f64(host_bits(out))
+    sent = ref["is_token_in_rank"].sum(-1) > 0
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(xf), 2.0 ** -126))) - 7)
+    assert np.all(np.abs(of - xf)[sent] <= 2 * ulp[sent])
+
+
+def test_empty_tokens():
+    R, T, H, E, k, C = 4, 0, 128, 8, 2, 3
+    inp = {"x": np.zeros((R, T, H), np.uint16), "topk_idx": np.zeros((R, T, k), np.int64),
+           "topk_weights": np.zeros((R, T, k), np.float32)}
+    run = GpuRun(R, T, H, E, k, C, inp)
+    got = run.layout()
+    ref = oracle.layout(inp["topk_idx"], E, C)
+    for key, arr in got.items():
+        np.testing.assert_array_equal(arr, ref[key], err_msg=key)
+
+
+def test_device_error_flags():
+    """Bad expert ids are skipped (as masked) and flagged; undersized receive regions
+    flag an overflow and skip the rows -- no fault, no trap."""
+    w = CASES["ragged"]
+    inp = workloads.make_workload(w)
+    bad = inp["topk_idx"].copy()
+    bad[0, 3, 1] = w.E
+    bad[2, 10, 0] = -5
+    inp2 = dict(inp, topk_idx=bad)
+    run = GpuRun(w.R, w.T, w.H, w.E, w.k, w.C, inp2)
+    got = run.layout()
+    assert run.flags() & ep.EP_DEVERR_BAD_EXPERT
+    ref = oracle.layout(bad, w.E, w.C)
+    assert ref["bad_entries"] == 2
+    for key, arr in got.items():
+        np.testing.assert_array_equal(arr, ref[key], err_msg=key)
+    # overflow: every region one row short
+    run.err.zero_()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    short = [0] + [off[d + 1] - (d + 1) for d in range(w.R)]
+    rb = run.dispatch(short)
+    assert run.flags() & ep.EP_DEVERR_RECV_OVERFLOW
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(short), w.E, bad, inp["topk_weights"],
+                          fill_x=0xA5A5, fill_idx=-99, fill_w=-5.0, fill_src=-3)
+    assert exp["bad_rows"] > 0
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb.recv_topk_idx), exp["recv_topk_idx"])
+
+
+# ----------------------------------------------------------------------------- low latency
+
+LL_CASES = {
+    "tiny": W("lt", R=2, T=128, H=256, E=8, k=2, nmax=128, seed=0),
+    "masked": W("lm", R=4, T=40, H=512, E=32, k=6, nmax=48, mask_p=0.05, seed=111),
+    "r8": W("l8", R=8, T=100, H=1024, E=64, k=8, nmax=128, mask_p=0.05, seed=112),
+}
+
+
+def _ll_setup(name):
+    w = LL_CASES[name]
+    inp = workloads.make_workload(w)
+    return w, inp, GpuRun(w.R, w.T, w.H, w.E, w.k, 1, inp, nmax=w.nmax)
+
+
+@pytest.mark.parametrize("name", list(LL_CASES))
+@pytest.mark.parametrize("use_fp8", [False, True])
+def test_ll_dispatch_bit_exact(name, use_fp8):
+    w, inp, run = _ll_setup(name)
+    buf = run.ll_dispatch(use_fp8)
+    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, use_fp8, fill_x=0x5A5A if not use_fp8 else 0x5A)
+    for key in ("slot", "recv_expert_count", "layout_range", "src_info"):
+        np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
+    np.testing.assert_array_equal(host_bits(buf.recv_x), exp["recv_x"])
+    if use_fp8:
+        filled = exp["src_info"] != -7
+        np.testing.assert_array_equal(host_bits(buf.recv_x_scales)[filled].view(np.uint32),
+                                      exp["recv_x_scales"][filled].view(np.uint32))
+    assert run.flags() == 0
+
+
+@pytest.mark.parametrize("name", list(LL_CASES))
+def test_ll_phase_split_equals_single_call(name):
+    w, inp, run = _ll_setup(name)
+    both = run.ll_dispatch(True)
+    split = run.ll_dispatch(True, phase=ep.EP_PHASE_SEND)
+    torch.cuda.synchronize()
+    run.ll_dispatch(True, phase=ep.EP_PHASE_RECV, buf=split)
+    for key in ("recv_x", "recv_x_scales", "src_info", "slot", "send_count", "recv_expert_count",
+                "layout_range"):
+        a, b = getattr(both, key), getattr(split, key)
+        if key == "recv_x_scales":
+            filled = (both.src_info != -7)
+            a, b = a[filled], b[filled]
+        assert torch.equal(a.view(torch.uint8) if a.dtype != torch.int32 else a,
+                           b.view(torch.uint8) if b.dtype != torch.int32 else b), key
+
+
+@pytest.mark.parametrize("name", list(LL_CASES))
+def test_ll_combine_within_tolerance(name):
+    w, inp, run = _ll_setup(name)
+    buf = run.ll_dispatch(False)
+    rng = np.random.default_rng(w.seed + 3000)
+    y32 = rng.standard_normal(tuple(buf.recv_x.shape)).astype(np.float32)
+    yb = torch.from_numpy(y32).to(torch.bfloat16)
+    out_send = run.ll_combine(yb.cuda(), buf, phase=ep.EP_PHASE_SEND)   # event-only phase
+    out = run.ll_combine(yb.cuda(), buf, phase=ep.EP_PHASE_RECV)
+    exp = oracle.ll_combine(yb.view(torch.int16).numpy().view(np.uint16), inp["topk_idx"],
+                            inp["topk_weights"], host_bits(buf.slot), w.E, w.nmax)
+    assert_close_bf16(host_bits(out), exp)
+    # identity experts: returns x * sum of valid weights (= x) within rounding
+    out2 = run.ll_combine(buf.recv_x, buf)
+    xf = bf16_to_f64(inp["x"]) * inp["topk_weights"].astype(np.float64).sum(-1)[..., None]
+    assert np.all(np.abs(bf16_to_f64(host_bits(out2)) - xf) <= 1e-3 + 1e-2 * np.abs(xf))
+    del out_send
+
+
+def test_ll_slot_overflow_flag():
+    """Duplicate experts in a token push a (source, expert) count past Nmax: flagged and
+    skipped exactly like the oracle, no fault."""
+    R, T, H, E, k, nmax = 2, 4, 128, 4, 2, 4
+    topk = np.zeros((R, T, k), np.int64)
+    rng = np.random.default_rng(113)
+    inp = {"x": workloads.make_hidden(rng, R, T, H), "topk_idx": topk,
+           "topk_weights": np.full((R, T, k), 0.5, np.float32)}
+    run = GpuRun(R, T, H, E, k, 1, inp, nmax=nmax)
+    buf = run.ll_dispatch(False)
+    assert run.flags() & ep.EP_DEVERR_SLOT_OVERFLOW
+    exp = oracle.ll_dispatch(inp["x"], topk, E, nmax, False)
+    assert exp["bad_entries"] == 2 * 4
+    np.testing.assert_array_equal(host_bits(buf.slot), exp["slot"])
+    np.testing.assert_array_equal(host_bits(buf.recv_expert_count), exp["recv_expert_count"])
