@@ -66,13 +66,19 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def source_digest():
+KERNEL_SOURCES = {
+    "dispatch_kernel<copy>": ("dispatch.cu", "rowops.cuh", "ep_internal.cuh"),
+    "combine_kernel": ("combine.cu", "rowops.cuh", "ep_internal.cuh"),
+}
+
+
+def source_digest(files):
+    """sha256 over the named kernel source files (and the C-ABI header)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_layout_02_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(files):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     with open(os.path.join(ROOT, "include", "ep.h"), "rb") as f:
         h.update(f.read())
     return h.hexdigest()
@@ -87,7 +93,9 @@ def traffic_from_profiles(kernel: str):
     with open(path) as f:
         entries = json.load(f)
     e = entries.get(kernel)
-    if not e or e.get("source_sha256") != source_digest():
+    if not e or kernel not in KERNEL_SOURCES:
+        return None
+    if e.get("source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -155,6 +163,61 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- our path
 
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_e2e(world, dev, stream, step, x, topk, wts, out, total_bytes, e2e_steps):
+    """The same step through the same C-ABI calls with host buffers: pinned host ->
+    device copies of x / topk_idx / topk_weights and a device -> host copy of the
+    combined output inside every timed step."""
+    import torch
+    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    x_h.copy_(x)
+    topk_h = torch.empty(topk.shape, dtype=topk.dtype, pin_memory=True)
+    topk_h.copy_(topk)
+    wts_h = torch.empty(wts.shape, dtype=wts.dtype, pin_memory=True)
+    wts_h.copy_(wts)
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        topk.copy_(topk_h, non_blocking=True)
+        wts.copy_(wts_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    h2d = x_h.numel() * x_h.element_size() + topk_h.numel() * 8 + wts_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+    return {"value": round(world * total_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
 def run_ours(args, rank, world):
     import torch
     import combine_layout_02_gb300 as ep
@@ -164,6 +227,8 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     ep.lib()                                              # fails loudly without libep.so
     w = WORKLOAD
+    if args.tokens:
+        w = workloads.Workload(w.name, R=w.R, T=args.tokens, H=w.H, E=w.E, k=w.k, C=w.C, seed=w.seed)
     R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
     inp = workloads.make_workload(w)
     sh = ep.make_shape(R, T, H, E, k, C)
@@ -202,14 +267,9 @@ def run_ours(args, rank, world):
     nbytes = algorithmic_bytes(R, T, H, k, N)
     total_bytes = sum(nbytes.values())
 
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
     def timed_region(sampler):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-        barrier()
+        barrier(world)
         torch.cuda.synchronize()
         n0 = ep.ep_kernel_launch_count()
         if sampler:
@@ -222,7 +282,7 @@ def run_ours(args, rank, world):
         t_end.record(stream)
         torch.cuda.synchronize()
         clocks = sampler.stop() if sampler else None
-        barrier()
+        barrier(world)
         launches = ep.ep_kernel_launch_count() - n0
         total_ms = t_start.elapsed_time(t_end)
         lay = [e[0].elapsed_time(e[1]) for e in evs]
@@ -238,51 +298,13 @@ def run_ours(args, rank, world):
         remeasured = True
         total_ms, lay, dis, com, launches, clocks = timed_region(ClockSampler(gpu_id))
 
-    ms_step = total_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = reduce_max(total_ms / args.steps, world, dev)
     flags = int(err.item())
     if flags != 0:
         raise RuntimeError(f"device error flags set: {flags}")
 
-    # ---- end to end through the C ABI with host buffers
-    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    x_h.copy_(x)
-    topk_h = torch.empty(topk.shape, dtype=topk.dtype, pin_memory=True)
-    topk_h.copy_(topk)
-    wts_h = torch.empty(wts.shape, dtype=wts.dtype, pin_memory=True)
-    wts_h.copy_(wts)
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    e2e_steps = max(3, min(args.steps, 20))
-
-    def e2e_step():
-        x.copy_(x_h, non_blocking=True)
-        topk.copy_(topk_h, non_blocking=True)
-        wts.copy_(wts_h, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    h2d = x_h.numel() * x_h.element_size() + topk_h.numel() * 8 + wts_h.numel() * 4
-    d2h = out_h.numel() * out_h.element_size()
+    e2e = None if args.no_e2e else run_e2e(world, dev, stream, step, x, topk, wts, out,
+                                           total_bytes, max(3, min(args.steps, 20)))
 
     peak, peak_kind = measured_peaks()
     dis_ms = statistics.mean(dis)
@@ -308,7 +330,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "dsv3: R=8 virtual ranks x 4096 tokens, hidden 7168 bf16, "
+        "config": {"workload": f"dsv3: R=8 virtual ranks x {T} tokens, hidden 7168 bf16, "
                                "256 experts (32/rank), top-8 distinct uniform, fp32 softmax "
                                "weights, 12 channels; layout + bf16 dispatch + weighted bf16 "
                                "combine (identity experts), worst-case receive capacity",
@@ -329,9 +351,7 @@ def run_ours(args, rank, world):
                      "peak_source": f"{peak_kind} hbm_gbs (copy)",
                      "traffic": traffic_from_profiles(dom_kernel),
                      "algorithmic_bytes_per_launch": nbytes[dom]},
-        "e2e": {"value": round(world * total_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+        "e2e": e2e,
         "gpu_launches": launches,
         "clocks": clocks,
         "clocks_remeasured": remeasured,
@@ -405,6 +425,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per source rank (default 4096); smaller cases are for "
+                         "profiler captures, not bench lines")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

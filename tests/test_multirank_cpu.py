@@ -1,0 +1,65 @@
+"""The benchmark's multi-rank path on CPU (gloo, world size 2): barrier, max-over-ranks
+timing and the reference arm's rank-0-only rule. The hot path itself does not shard
+(the virtual ranks live in one GPU's memory), so N > 1 means independent replicas."""
+import multiprocessing as mp
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            init_method=f"tcp://127.0.0.1:{port}")
+    import bench
+    mx = bench.reduce_max(float(10 * (rank + 1)), world)
+    bench.barrier(world)
+
+    class A:
+        steps, warmup = 1, 0
+    ref = bench.run_reference(A, rank, world) if rank != 0 else "skipped"
+    q.put((rank, mx, ref))
+    dist.destroy_process_group()
+
+
+def test_reduce_max_and_reference_rank_rule_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [20.0, 20.0]
+    assert res[1][2] is None          # non-zero ranks of the reference arm do no work
+
+
+def test_reduce_max_single_rank_is_identity():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max(3.5, 1) == 3.5
+
+
+def test_bytes_model_counts_each_byte_once():
+    sys.path.insert(0, ROOT)
+    import bench
+    b = bench.algorithmic_bytes(R=8, T=4096, H=7168, k=8, N=173_000)
+    # payload: x read once + N rows written (dispatch); N rows read + x written (combine)
+    assert b["dispatch"] - (8 * 4096 * 7168 * 2 + 173_000 * 7168 * 2) == \
+        8 * 4096 * (8 * 12 + 8 * 4) + 173_000 * (8 * 12 + 4)
+    assert b["combine"] - (173_000 * 7168 * 2 + 8 * 4096 * 7168 * 2) == \
+        8 * 4096 * 8 * 4 + 8 * 4096 * 8 * 12
