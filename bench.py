@@ -73,14 +73,12 @@ KERNEL_SOURCES = {
 
 
 def source_digest(files):
-    """sha256 over the named kernel source files (and the C-ABI header)."""
+    """sha256 over the named kernel source files."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_layout_02_gb300", "csrc")
     for name in sorted(files):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
-    with open(os.path.join(ROOT, "include", "ep.h"), "rb") as f:
-        h.update(f.read())
     return h.hexdigest()
 
 
