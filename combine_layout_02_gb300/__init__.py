@@ -24,8 +24,8 @@ __all__ = [
     "EP_PHASE_SEND", "EP_PHASE_RECV", "EP_PHASE_BOTH", "EP_MAX_RANKS",
     "EpError", "ep_shape", "ep_launch", "ep_layout", "ep_handle", "ep_recv", "ep_ll_buffer",
     "lib", "library_path", "make_shape", "make_launch",
-    "ep_layout_workspace_size", "ep_get_layout", "ep_dispatch", "ep_combine",
-    "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
+    "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
+    "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
     "ep_read_error_flags_sync", "ep_kernel_launch_count", "ep_abi_version",
     "EXPORTED_SYMBOLS",
 ]
@@ -39,7 +39,8 @@ EP_MAX_RANKS = 64
 
 # Every function include/ep.h declares (checked by the ABI test).
 EXPORTED_SYMBOLS = (
-    "ep_layout_workspace_size", "ep_get_layout", "ep_dispatch", "ep_combine",
+    "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
+    "ep_dispatch", "ep_combine",
     "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
     "ep_read_error_flags_sync", "ep_status_string", "ep_last_cuda_error",
     "ep_kernel_launch_count", "ep_abi_version",
@@ -110,6 +111,8 @@ def lib():
         L.ep_layout_workspace_size.restype = ctypes.c_size_t
         L.ep_get_layout.argtypes = [S(ep_shape), _P, S(ep_layout), S(ep_handle), _P,
                                     ctypes.c_size_t, S(ep_launch)]
+        L.ep_get_layout_static_scratch.argtypes = [S(ep_shape), _P, S(ep_layout), S(ep_handle),
+                                                   S(ep_launch)]
         L.ep_dispatch.argtypes = [S(ep_shape), _P, ctypes.c_int, _P, ctypes.c_int, _P, _P,
                                   S(ep_handle), S(ep_recv), S(ep_launch)]
         L.ep_combine.argtypes = [S(ep_shape), _P, _P, S(ep_handle), ctypes.c_int, _P, _P, _P,
@@ -129,7 +132,7 @@ def lib():
         L.ep_kernel_launch_count.restype = ctypes.c_uint64
         L.ep_abi_version.argtypes = []
         L.ep_abi_version.restype = _I32
-        for name in ("ep_get_layout", "ep_dispatch", "ep_combine", "ep_ll_dispatch",
+        for name in ("ep_get_layout", "ep_get_layout_static_scratch", "ep_dispatch", "ep_combine", "ep_ll_dispatch",
                      "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
                      "ep_read_error_flags_sync"):
             getattr(L, name).restype = _I32
@@ -204,6 +207,17 @@ def ep_get_layout(shape: ep_shape, topk_idx, layout: Optional[ep_layout], handle
                          workspace.numel() * workspace.element_size(),
                          ctypes.byref(_launch(launch)))
     _check("ep_get_layout", st)
+
+
+def ep_get_layout_static_scratch(shape: ep_shape, topk_idx, layout: Optional[ep_layout],
+                                 handle: ep_handle, launch: Optional[ep_launch] = None) -> None:
+    """ep_get_layout for callers that cannot allocate device memory: the workspace is a
+    fixed array inside libep.so (EP_LAYOUT_STATIC_SCRATCH_BYTES). Calls on one device
+    share it, so calls that may run at the same time on the GPU must be ordered."""
+    st = lib().ep_get_layout_static_scratch(ctypes.byref(shape), _ptr(topk_idx),
+                                            ctypes.byref(layout) if layout is not None else None,
+                                            ctypes.byref(handle), ctypes.byref(_launch(launch)))
+    _check("ep_get_layout_static_scratch", st)
 
 
 def _offsets(row_offset: Sequence[int]):

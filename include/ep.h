@@ -210,6 +210,30 @@ EP_API ep_status ep_get_layout(const ep_shape* shape, const int64_t* topk_idx, e
                         ep_handle* handle, void* workspace, size_t workspace_bytes,
                         const ep_launch* launch);
 
+/* Size of the fixed device scratch array used by ep_get_layout_static_scratch. */
+#define EP_LAYOUT_STATIC_SCRATCH_BYTES (256 * 1024)
+
+/* ep_get_layout without a workspace argument, for callers that cannot allocate device
+ * memory (for example a plugin whose host framework owns all device memory through its
+ * own pool, or a latency-critical path where cudaMalloc / cudaFree would synchronise
+ * the device). The pages have no counterpart: it exists only because the layout
+ * kernels need scratch. Same outputs, status codes and ordering as ep_get_layout.
+ *   - The scratch is a file-scope device array of EP_LAYOUT_STATIC_SCRATCH_BYTES bytes
+ *     inside libep.so; every GPU that loads the library holds it until the process
+ *     exits. Shapes whose ep_layout_workspace_size exceeds it return
+ *     EP_ERR_UNSUPPORTED before anything is enqueued (R=8, C=12, E=256 needs ~96 KiB).
+ *   - The first call on a device (with that device current) looks up the array's
+ *     device address; make that first call before any stream capture.
+ *   - The call itself allocates nothing and frees nothing.
+ *   - All calls on a device share the one array. Calls whose kernels may overlap on
+ *     the GPU (different streams without ordering between them) race on it and give
+ *     wrong results; order them, or use ep_get_layout with separate workspaces.
+ *     Stale contents from an earlier call are harmless: every word read is first
+ *     written by the same call. */
+EP_API ep_status ep_get_layout_static_scratch(const ep_shape* shape, const int64_t* topk_idx,
+                                              ep_layout* layout, ep_handle* handle,
+                                              const ep_launch* launch);
+
 /* ---------------------------------------------------------------- dispatch */
 
 /* dispatch ([README] normal-kernel example, dispatch_forward / combine_backward;
