@@ -216,57 +216,165 @@ def run_e2e(world, dev, stream, step, x, topk, wts, out, total_bytes, e2e_steps)
             "d2h_bytes_per_step": d2h}
 
 
+PHASE_KERNEL = {"dispatch": "dispatch_kernel<copy>", "dispatch_fp8": "dispatch_kernel<quant>",
+                "combine": "combine_kernel", "layout": "layout_count+layout_prefix",
+                "ll_send": "ll_send_kernel", "ll_recv": "ll_recv_kernel",
+                "ll_combine": "ll_combine_kernel"}
+
+WORKLOAD_TEXT = {
+    "dsv3": "R=8 virtual ranks x {T} tokens, hidden 7168 bf16, 256 experts (32/rank), top-8 "
+            "distinct uniform, fp32 softmax weights, 12 channels; layout + bf16 dispatch + "
+            "weighted bf16 combine (identity experts), worst-case receive capacity",
+    "group_limited": "dsv3 shape, 4-of-8 expert groups then top-8 inside them; layout + fused "
+                     "e4m3 dispatch (per-128-channel fp32 scales) + weighted bf16 combine",
+    "ll_decode": "R=8 x {T} tokens, hidden 7168, 256 experts, top-8 with 5% masked; low-latency "
+                 "e4m3 dispatch send phase, receive phase, weighted bf16 combine; Nmax=128",
+    "zipf_reuse": "R=16 x {T} tokens, hidden 4096, 128 experts, top-6 Zipf(1.2); layout once, "
+                  "then dispatch(handle) of fresh x + weighted combine(handle)",
+}
+
+
+def make_plan(args, ep, dev, stream, launch):
+    """Device buffers and the step of one workload: a list of (phase, call) pairs, plus a
+    function giving each phase's algorithmic bytes once the layout is known."""
+    import dataclasses
+    import torch
+    from combine_layout_02_gb300.buffers import (LayoutBuffers, LLBuffers, RecvBuffers,
+                                                 worst_case_row_offsets)
+    w = workloads.CONFIGS[args.workload]
+    if args.tokens:
+        w = dataclasses.replace(w, T=args.tokens)
+    R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
+    inp = workloads.make_workload(w)
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(inp["topk_idx"]).to(dev)
+    wts = torch.from_numpy(inp["topk_weights"]).to(dev)
+    Tt = R * T
+    plan = {"w": w, "inp": inp, "x": x, "topk": topk, "wts": wts, "flush": False}
+
+    if args.workload in ("dsv3", "group_limited", "zipf_reuse"):
+        sh = ep.make_shape(R, T, H, E, k, C)
+        off = worst_case_row_offsets(R, T)
+        lb = LayoutBuffers(sh, dev)
+        fp8 = args.workload == "group_limited"
+        reuse = args.workload == "zipf_reuse"
+        rb = RecvBuffers(off[-1], H, k, recv_dtype=ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16,
+                         with_topk=not reuse, device=dev)
+        out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+        layout_s, handle = lb.layout(), lb.handle(rb.recv_src_idx)
+
+        def layout():
+            ep.ep_get_layout(sh, topk, layout_s, handle, lb.workspace, launch)
+
+        if fp8:
+            # bf16 expert outputs for the combine: the bf16 rows of the same routing
+            y = RecvBuffers(off[-1], H, k, with_topk=False, device=dev).recv_x
+            layout()
+            ep.ep_dispatch(sh, x, ep.EP_BF16, None, ep.EP_BF16, None, None, handle, y, None,
+                           None, None, None, off, launch)
+        else:
+            y = rb.recv_x
+        xs = [x]
+        if reuse:
+            layout()      # once, outside the timed steps
+            rng = np.random.default_rng(w.seed + 77)
+            xs.append(torch.from_numpy(workloads.make_hidden(rng, R, T, H).view(np.int16))
+                      .to(dev).view(torch.bfloat16))
+        it = [0]
+
+        def dispatch():
+            xi = xs[it[0] % len(xs)]
+            it[0] += 1
+            if reuse:
+                ep.ep_dispatch(sh, xi, ep.EP_BF16, None, ep.EP_BF16, None, None, handle, rb.recv_x,
+                               None, None, None, rb.recv_src_idx, off, launch)
+            else:
+                ep.ep_dispatch(sh, xi, ep.EP_BF16, None, ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16,
+                               topk, wts, handle, rb.recv_x, rb.recv_x_scales, rb.recv_topk_idx,
+                               rb.recv_topk_weights, rb.recv_src_idx, off, launch)
+
+        def combine():
+            ep.ep_combine(sh, y, off, handle, ep.EP_COMBINE_WEIGHTED, topk, wts, None, out, None,
+                          launch)
+
+        dname = "dispatch_fp8" if fp8 else "dispatch"
+        plan["phases"] = ([] if reuse else [("layout", layout)]) + [(dname, dispatch), ("combine", combine)]
+        plan["out"] = out
+
+        def nbytes():
+            N = int(lb.rank_prefix_matrix[-1].sum().item())
+            lay = Tt * k * 8 + Tt * R * (1 + 4)
+            meta_in = Tt * R * 4 + (0 if reuse else Tt * k * 12)
+            meta_out = N * 4 + (0 if reuse else N * k * 12)
+            payload = N * H * (1 if fp8 else 2) + (N * (H // 128) * 4 if fp8 else 0)
+            b = {dname: Tt * H * 2 + payload + meta_in + meta_out,
+                 "combine": N * H * 2 + Tt * H * 2 + Tt * R * 4 + Tt * k * 12}
+            if not reuse:
+                b["layout"] = lay
+            return b, N
+        plan["nbytes"] = nbytes
+        plan["l2"] = "inputs larger than L2; no flush"
+    elif args.workload == "ll_decode":
+        sh = ep.make_shape(R, T, H, E, k, C, nmax=w.nmax)
+        buf = LLBuffers(sh, True, device=dev)
+        ybuf = LLBuffers(sh, False, device=dev)
+        ep.ep_ll_dispatch(sh, x, topk, False, ep.EP_PHASE_BOTH, ybuf.struct(), launch)
+        out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+        s_buf, s_y = buf.struct(), ybuf.struct()
+        plan["phases"] = [
+            ("ll_send", lambda: ep.ep_ll_dispatch(sh, x, topk, True, ep.EP_PHASE_SEND, s_buf, launch)),
+            ("ll_recv", lambda: ep.ep_ll_dispatch(sh, x, topk, True, ep.EP_PHASE_RECV, s_buf, launch)),
+            ("ll_combine", lambda: ep.ep_ll_combine(sh, ybuf.recv_x, topk, wts, s_y,
+                                                    ep.EP_PHASE_RECV, out, launch)),
+        ]
+        plan["flush"] = True
+        plan["l2"] = "L2 flushed before every step (a 512 MB buffer is zeroed outside the timed kernels)"
+
+        def nbytes():
+            M = int((inp["topk_idx"] >= 0).sum())
+            G = H // 128
+            return {"ll_send": Tt * H * 2 + M * (H + G * 4) + Tt * k * (8 + 4) + M * 4 + E * R * 4,
+                    "ll_recv": E * R * 4 + E * R * 8 + E * 4,
+                    "ll_combine": M * H * 2 + Tt * H * 2 + Tt * k * (8 + 4 + 4)}, M
+        plan["nbytes"] = nbytes
+    else:
+        raise ValueError(args.workload)
+    return plan
+
+
 def run_ours(args, rank, world):
     import torch
     import combine_layout_02_gb300 as ep
-    from combine_layout_02_gb300.buffers import LayoutBuffers, RecvBuffers, worst_case_row_offsets
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     ep.lib()                                              # fails loudly without libep.so
-    w = WORKLOAD
-    if args.tokens:
-        w = workloads.Workload(w.name, R=w.R, T=args.tokens, H=w.H, E=w.E, k=w.k, C=w.C, seed=w.seed)
-    R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
-    inp = workloads.make_workload(w)
-    sh = ep.make_shape(R, T, H, E, k, C)
-
-    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
-    topk = torch.from_numpy(inp["topk_idx"]).to(dev)
-    wts = torch.from_numpy(inp["topk_weights"]).to(dev)
-    off = worst_case_row_offsets(R, T)
-    lb = LayoutBuffers(sh, dev)
-    rb = RecvBuffers(off[-1], H, k, device=dev)
-    out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
     launch = ep.make_launch(stream, error_flags=err)
-    layout_s, handle = lb.layout(), lb.handle(rb.recv_src_idx)
+    plan = make_plan(args, ep, dev, stream, launch)
+    phases = plan["phases"]
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if plan["flush"] else None
 
     def step(ev=None):
+        for i, (_, call) in enumerate(phases):
+            if ev is not None:
+                ev[i].record(stream)
+            call()
         if ev is not None:
-            ev[0].record(stream)
-        ep.ep_get_layout(sh, topk, layout_s, handle, lb.workspace, launch)
-        if ev is not None:
-            ev[1].record(stream)
-        ep.ep_dispatch(sh, x, ep.EP_BF16, None, ep.EP_BF16, topk, wts, handle, rb.recv_x, None,
-                       rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx, off, launch)
-        if ev is not None:
-            ev[2].record(stream)
-        ep.ep_combine(sh, rb.recv_x, off, handle, ep.EP_COMBINE_WEIGHTED, topk, wts, None, out,
-                      None, launch)
-        if ev is not None:
-            ev[3].record(stream)
+            ev[len(phases)].record(stream)
 
     for _ in range(max(args.warmup, 3)):
+        if flush_buf is not None:
+            flush_buf.zero_()
         step()
     torch.cuda.synchronize()
-    N = int(lb.rank_prefix_matrix[-1].sum().item())
-    nbytes = algorithmic_bytes(R, T, H, k, N)
+    nbytes, units = plan["nbytes"]()
     total_bytes = sum(nbytes.values())
 
     def timed_region(sampler):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)]
+               for _ in range(args.steps)]
         barrier(world)
         torch.cuda.synchronize()
         n0 = ep.ep_kernel_launch_count()
@@ -276,44 +384,42 @@ def run_ours(args, rank, world):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(args.steps):
+            if flush_buf is not None:
+                flush_buf.zero_()
             step(evs[i])
         t_end.record(stream)
         torch.cuda.synchronize()
         clocks = sampler.stop() if sampler else None
         barrier(world)
         launches = ep.ep_kernel_launch_count() - n0
-        total_ms = t_start.elapsed_time(t_end)
-        lay = [e[0].elapsed_time(e[1]) for e in evs]
-        dis = [e[1].elapsed_time(e[2]) for e in evs]
-        com = [e[2].elapsed_time(e[3]) for e in evs]
-        return total_ms, lay, dis, com, launches, clocks
+        per = {name: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, (name, _) in enumerate(phases)}
+        total_ms = (sum(sum(v) for v in per.values()) if flush_buf is not None
+                    else t_start.elapsed_time(t_end))
+        return total_ms, per, launches, clocks
 
     gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     gpu_id = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
     remeasured = False
-    total_ms, lay, dis, com, launches, clocks = timed_region(ClockSampler(gpu_id))
+    total_ms, per, launches, clocks = timed_region(ClockSampler(gpu_id))
     if clocks and any(r in clocks["reasons"] for r in BAD_REASONS):
         remeasured = True
-        total_ms, lay, dis, com, launches, clocks = timed_region(ClockSampler(gpu_id))
+        total_ms, per, launches, clocks = timed_region(ClockSampler(gpu_id))
 
     ms_step = reduce_max(total_ms / args.steps, world, dev)
     flags = int(err.item())
     if flags != 0:
         raise RuntimeError(f"device error flags set: {flags}")
 
-    e2e = None if args.no_e2e else run_e2e(world, dev, stream, step, x, topk, wts, out,
-                                           total_bytes, max(3, min(args.steps, 20)))
+    e2e = None
+    if args.workload == "dsv3" and not args.no_e2e:
+        e2e = run_e2e(world, dev, stream, step, plan["x"], plan["topk"], plan["wts"], plan["out"],
+                      total_bytes, max(3, min(args.steps, 20)))
 
     peak, peak_kind = measured_peaks()
-    dis_ms = statistics.mean(dis)
-    com_ms = statistics.mean(com)
-    lay_ms = statistics.mean(lay)
-    dis_gbs = nbytes["dispatch"] / (dis_ms * 1e6)
-    com_gbs = nbytes["combine"] / (com_ms * 1e6)
-    if dis_ms >= com_ms:
-        dom, dom_gbs, dom_kernel = "dispatch", dis_gbs, "dispatch_kernel<copy>"
-    else:
-        dom, dom_gbs, dom_kernel = "combine", com_gbs, "combine_kernel"
+    w = plan["w"]
+    mean_ms = {name: statistics.mean(v) for name, v in per.items()}
+    gbs = {name: nbytes[name] / (mean_ms[name] * 1e6) for name in mean_ms}
+    dom = max(mean_ms, key=lambda n: mean_ms[n])
     value = world * total_bytes / (ms_step * 1e6)
     result = {
         "metric": METRIC,
@@ -328,33 +434,32 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"dsv3: R=8 virtual ranks x {T} tokens, hidden 7168 bf16, "
-                               "256 experts (32/rank), top-8 distinct uniform, fp32 softmax "
-                               "weights, 12 channels; layout + bf16 dispatch + weighted bf16 "
-                               "combine (identity experts), worst-case receive capacity",
-                   "R": R, "T": T, "H": H, "E": E, "k": k, "C": C, "recv_rows": N,
-                   "parallelism": f"replicas x{world} (virtual EP8 inside each GPU)",
-                   "l2": "inputs larger than L2 (x 470 MB, recv_x 2.49 GB); no flush"},
-        "dispatch_gbs": round(dis_gbs, 1),
-        "combine_gbs": round(com_gbs, 1),
-        "dispatch_frac_of_peak": round(dis_gbs / peak, 4),
-        "combine_frac_of_peak": round(com_gbs / peak, 4),
-        "layout_us": round(lay_ms * 1e3, 2),
-        "dispatch_us": round(dis_ms * 1e3, 2),
-        "combine_us": round(com_ms * 1e3, 2),
-        "layout_dispatch_us": round((lay_ms + dis_ms) * 1e3, 2),
-        "bytes_per_step": nbytes,
-        "roofline": {"bound": "hbm", "kernel": dom_kernel, "achieved": round(dom_gbs, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(dom_gbs / peak, 4),
-                     "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                     "traffic": traffic_from_profiles(dom_kernel),
-                     "algorithmic_bytes_per_launch": nbytes[dom]},
-        "e2e": e2e,
-        "gpu_launches": launches,
-        "clocks": clocks,
-        "clocks_remeasured": remeasured,
+        "config": {"workload": f"{args.workload}: " + WORKLOAD_TEXT[args.workload].format(T=w.T),
+                   "R": w.R, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "C": w.C,
+                   "recv_rows" if args.workload != "ll_decode" else "valid_entries": units,
+                   "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)",
+                   "l2": plan["l2"]},
     }
-    return result, inp
+    for name in mean_ms:
+        short = name.replace("_fp8", "")
+        result[f"{short}_us"] = round(mean_ms[name] * 1e3, 2)
+        if name != "layout" and name != "ll_recv":
+            result[f"{short}_gbs"] = round(gbs[name], 1)
+            result[f"{short}_frac_of_peak"] = round(gbs[name] / peak, 4)
+    if "layout" in mean_ms:
+        dname = "dispatch_fp8" if "dispatch_fp8" in mean_ms else "dispatch"
+        result["layout_dispatch_us"] = round((mean_ms["layout"] + mean_ms[dname]) * 1e3, 2)
+    result["bytes_per_step"] = nbytes
+    result["roofline"] = {"bound": "hbm", "kernel": PHASE_KERNEL[dom], "achieved": round(gbs[dom], 1),
+                          "peak": peak, "unit": "GB/s", "frac": round(gbs[dom] / peak, 4),
+                          "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                          "traffic": traffic_from_profiles(PHASE_KERNEL[dom]),
+                          "algorithmic_bytes_per_launch": nbytes[dom]}
+    result["e2e"] = e2e
+    result["gpu_launches"] = launches
+    result["clocks"] = clocks
+    result["clocks_remeasured"] = remeasured
+    return result, plan["inp"]
 
 
 # ----------------------------------------------------------------------------- oracle
@@ -424,6 +529,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="dsv3",
+                    help="dsv3 is the benchmark line; the others are extra measurements")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per source rank (default 4096); smaller cases are for "
                          "profiler captures, not bench lines")
@@ -447,7 +554,7 @@ def main():
         dist.init_process_group(backend)
 
     res, inp = run_ours(args, rank, world)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == "dsv3":
         gbs, desc, _ = oracle_sample(inp, 2, budget_s=20.0)
         res["cpu_baseline"] = {"value": round(gbs, 3), "unit": "GB/s", "cores": 1,
                                "kind": "oracle", "sample": desc}

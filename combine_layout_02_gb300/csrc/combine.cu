@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
     __shared__ float s_coef[kWarps][EP_MAX_RANKS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kWarps;
+    pdl_wait();
 
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
         int nd = 0;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
                              a.out + g * (int64_t)a.H * 2, lane, 32);
         __syncwarp();
     }
+    pdl_trigger();
 }
 
 }  // namespace
@@ -135,8 +137,9 @@ extern "C" ep_status ep_combine(const ep_shape* sh, const void* y, const int64_t
             const int64_t cap = (int64_t)sh->num_sms * (per_sm > 0 ? per_sm : 1);
             if (blocks > cap) blocks = cap;
         }
-        combine_kernel<2><<<(unsigned)blocks, kThreads, 0, launch->stream>>>(a);
-        count_launches(1);
+        cudaError_t e = launch_pdl(combine_kernel<2>, dim3((unsigned)blocks), dim3(kThreads), 0,
+                                   launch->stream, a);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);
 }

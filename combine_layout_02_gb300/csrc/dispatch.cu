@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
     const int64_t nw = (int64_t)gridDim.x * kWarps;
     const int64_t out_row_bytes = (int64_t)a.H * (MODE == kQuant ? 1 : a.in_elem);
     const int G = a.H >> 7;
+    pdl_wait();
 
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
         const int t = (int)(g % a.T);
@@ -111,6 +112,7 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
         }
         __syncwarp();
     }
+    pdl_trigger();
 }
 
 template <int MODE, int U>
@@ -125,9 +127,8 @@ ep_status launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t strea
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    dispatch_kernel<MODE, U><<<(unsigned)blocks, kThreads, 0, stream>>>(a);
-    count_launches(1);
-    return EP_OK;
+    cudaError_t e = launch_pdl(dispatch_kernel<MODE, U>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
+    return e == cudaSuccess ? EP_OK : cuda_fail(e);
 }
 
 }  // namespace

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/ep.h"
 
 namespace ep {
@@ -70,6 +72,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
+// Programmatic dependent launch. Every kernel of the library calls pdl_wait() before
+// its first global-memory access, so a kernel launched early (while the previous kernel
+// of the stream still runs) only overlaps its launch latency, never its memory work.
+// pdl_trigger() lets the next kernel of the stream start launching. Both are no-ops
+// for kernels launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Destination-row regions passed by value (host array copied into kernel params).
 struct RowOffsets {
     int64_t v[EP_MAX_RANKS + 1];
@@ -99,5 +111,25 @@ void count_launches(uint64_t n);
 ep_status load_row_offsets(const int64_t* host, int R, RowOffsets* out);
 
 inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Launches `kernel` on `stream` with programmatic stream serialization allowed (see
+// pdl_wait / pdl_trigger) and counts the launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    if (e == cudaSuccess) count_launches(1);
+    return e;
+}
 
 }  // namespace ep

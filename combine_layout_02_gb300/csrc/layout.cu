@@ -76,8 +76,10 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
     int* hist = smem;          // [E]
     int* cnt = smem + a.E;     // [R]
     const int c = blockIdx.x, s = blockIdx.y, lane = threadIdx.x & 31;
+    pdl_trigger();   // tiny kernel: let the prefix kernel launch right away
     for (int i = threadIdx.x; i < a.E; i += kThreads) hist[i] = 0;
     for (int i = threadIdx.x; i < a.R; i += kThreads) cnt[i] = 0;
+    pdl_wait();
     __syncthreads();
 
     const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
@@ -86,15 +88,21 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
         uint64_t mask = 0;
         if (t < t1) {
             const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t) * a.k;
-            for (int j = 0; j < a.k; ++j) {
-                const int64_t e = row[j];
-                if (e == -1) continue;
-                if (e < 0 || e >= a.E) {
-                    raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
-                    continue;
+            for (int j0 = 0; j0 < a.k; j0 += 8) {
+                // Issue the token's loads together, then use them.
+                int64_t e[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) e[i] = (j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (e[i] == -1) continue;
+                    if (e[i] < 0 || e[i] >= a.E) {
+                        raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
+                        continue;
+                    }
+                    atomicAdd(&hist[(int)e[i]], 1);
+                    mask |= 1ull << ((int)e[i] / a.E_loc);
                 }
-                atomicAdd(&hist[(int)e], 1);
-                mask |= 1ull << ((int)e / a.E_loc);
             }
             const int64_t off = ((int64_t)s * a.T + t) * a.R;
             write_rank_bytes(a.in_rank + off, mask, a.R);
@@ -119,11 +127,14 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
     const int c = blockIdx.x, s = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = a.R, C = a.C, E = a.E;
+    pdl_trigger();
+    pdl_wait();
 
     // (1) One warp per destination d: A = tokens of earlier sources, B = tokens of
     // earlier channels of s, own = this channel, F = all channels of s.
     for (int d = warp; d < R; d += kWarps) {
         int A = 0, B = 0, own = 0, F = 0;
+#pragma unroll 4
         for (int i = lane; i < s * C; i += 32) {
             const int sp = i / C, cp = i - sp * C;
             A += a.ws_cnt[((int64_t)sp * R + d) * C + cp];
@@ -155,12 +166,14 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
         for (int p = b * kThreads + threadIdx.x; p < R * E; p += nblocks * kThreads) {
             const int sp = p / E, e = p - sp * E;
             int sum = 0;
+#pragma unroll 4
             for (int cp = 0; cp < C; ++cp) sum += a.ws_expert[((int64_t)sp * C + cp) * E + e];
             a.num_tokens_per_expert[p] = sum;
         }
     }
     for (int e = b * kWarps + warp; e < E; e += nblocks * kWarps) {
         int sum = 0;
+#pragma unroll 4
         for (int i = lane; i < R * C; i += 32) sum += a.ws_expert[(int64_t)i * E + e];
         sum = warp_sum(sum);
         if (lane == 0) a.num_recv_per_expert[e] = sum;
@@ -267,9 +280,10 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     if ((st = begin_call(launch)) != EP_OK) return st;
     const dim3 grid(a.C, a.R);
     const size_t smem = sizeof(int) * (size_t)(a.E + a.R);
-    layout_count_kernel<<<grid, kThreads, smem, launch->stream>>>(a);
-    layout_prefix_kernel<<<grid, kThreads, 0, launch->stream>>>(a);
-    count_launches(2);
+    cudaError_t e = launch_pdl(layout_count_kernel, grid, dim3(kThreads), smem, launch->stream, a);
+    if (e == cudaSuccess)
+        e = launch_pdl(layout_prefix_kernel, grid, dim3(kThreads), 0, launch->stream, a);
+    if (e != cudaSuccess) return cuda_fail(e);
     return end_call(launch);
 }
 

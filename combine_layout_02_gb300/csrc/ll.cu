@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     extern __shared__ int hist[];   // [E], count blocks only
     const int b = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
+    pdl_wait();
 
     if (b >= a.R * a.T) {
         const int s = b - a.R * a.T;
@@ -66,6 +67,7 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
         __syncthreads();
         for (int e = threadIdx.x; e < a.E; e += kThreads)
             a.send_count[(int64_t)e * a.R + s] = min(hist[e], a.nmax);   // e = d*E_loc + el
+        pdl_trigger();
         return;
     }
 
@@ -123,11 +125,14 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
                              a.H, threadIdx.x, kThreads);
     else
         scatter_copy_row<2>(src, a.recv_x, s_rows, s_nv, (int64_t)a.H * 2, threadIdx.x, kThreads);
+    pdl_trigger();
 }
 
 // One thread per (destination rank, local expert) = expert e.
 __global__ void __launch_bounds__(kThreads) ll_recv_kernel(LLArgs a) {
     const int e = blockIdx.x * kThreads + threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     if (e >= a.E) return;
     int total = 0;
     for (int s = 0; s < a.R; ++s) {
@@ -146,6 +151,7 @@ __global__ void __launch_bounds__(kThreads) ll_combine_kernel(LLArgs a) {
     __shared__ int s_nv;
     const int64_t tok = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
+    pdl_wait();
     if (threadIdx.x < a.k) {
         const int j = threadIdx.x;
         const int64_t e = a.topk_idx[tok * a.k + j];
@@ -171,6 +177,7 @@ __global__ void __launch_bounds__(kThreads) ll_combine_kernel(LLArgs a) {
     }
     __syncthreads();
     gather_reduce_row<1>(a.y, s_rows, s_w, s_nv, a.H, a.out + tok * (int64_t)a.H * 2, threadIdx.x, kThreads);
+    pdl_trigger();
 }
 
 ep_status ll_common_checks(const ep_shape* sh, const ep_launch* launch) {
@@ -230,12 +237,14 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (phase & EP_PHASE_SEND) {
         const unsigned blocks = (unsigned)(a.R * a.T + a.R);
-        ll_send_kernel<<<blocks, kThreads, sizeof(int) * (size_t)a.E, launch->stream>>>(a);
-        count_launches(1);
+        cudaError_t e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads),
+                                   sizeof(int) * (size_t)a.E, launch->stream, a);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     if (phase & EP_PHASE_RECV) {
-        ll_recv_kernel<<<(unsigned)ceil_div(a.E, kThreads), kThreads, 0, launch->stream>>>(a);
-        count_launches(1);
+        cudaError_t e = launch_pdl(ll_recv_kernel, dim3((unsigned)ceil_div(a.E, kThreads)),
+                                   dim3(kThreads), 0, launch->stream, a);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);
 }
@@ -272,8 +281,9 @@ ep_status ep_ll_combine(const ep_shape* sh, const void* y, const int64_t* topk_i
     // Send phase: in one device memory the return transfer is nothing; the call only
     // orders the stream (wait_event) and records the completion event.
     if ((phase & EP_PHASE_RECV) && a.R * a.T > 0) {
-        ll_combine_kernel<<<(unsigned)(a.R * a.T), kThreads, 0, launch->stream>>>(a);
-        count_launches(1);
+        cudaError_t e = launch_pdl(ll_combine_kernel, dim3((unsigned)(a.R * a.T)), dim3(kThreads), 0,
+                                   launch->stream, a);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);
 }
