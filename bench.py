@@ -244,6 +244,8 @@ def make_plan(args, ep, dev, stream, launch):
     w = workloads.CONFIGS[args.workload]
     if args.tokens:
         w = dataclasses.replace(w, T=args.tokens)
+    if args.nmax:
+        w = dataclasses.replace(w, nmax=args.nmax)
     R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
     inp = workloads.make_workload(w)
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
@@ -531,6 +533,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="dsv3",
                     help="dsv3 is the benchmark line; the others are extra measurements")
+    ap.add_argument("--nmax", type=int, default=0,
+                    help="low-latency slot capacity override (profiler captures only)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per source rank (default 4096); smaller cases are for "
                          "profiler captures, not bench lines")

@@ -19,6 +19,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+// Gather batch: P rows x U 16-byte units per lane in flight (best measured on GB300
+// among U in {1,2,4} x P in {4,8}).
+constexpr int kU = 4, kP = 4;
 
 struct CombineArgs {
     const char* y;
@@ -34,7 +37,7 @@ struct CombineArgs {
     uint32_t* err;
 };
 
-template <int U>
+template <int U, int P>
 __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
     __shared__ float s_coef[kWarps][EP_MAX_RANKS];
@@ -43,11 +46,20 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
     pdl_wait();
 
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
+        // Every metadata load of the token is issued at once: lanes < k read the token's
+        // expert ids and weights, lanes < R its send_head entries. The coefficient of
+        // rank d is then a sum over warp shuffles (entries in ascending order).
+        int rank_j = -1;
+        float w_j = 0.0f;
+        if (a.weighted && lane < a.k) {
+            const int64_t e = a.topk_idx[g * a.k + lane];
+            w_j = a.topk_weights[g * a.k + lane];
+            rank_j = e >= 0 ? (int)(e / a.E_loc) : -1;
+        }
         int nd = 0;
         for (int d0 = 0; d0 < a.R; d0 += 32) {
             const int d = d0 + lane;
             int64_t row = -1;
-            float coef = 1.0f;
             if (d < a.R) {
                 const int h = a.send_head[g * a.R + d];
                 if (h >= 0) {
@@ -57,12 +69,14 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
                         row = -1;
                     }
                 }
-                if (row >= 0 && a.weighted) {
-                    coef = 0.0f;
-                    for (int j = 0; j < a.k; ++j) {
-                        const int64_t e = a.topk_idx[g * a.k + j];
-                        if (e >= 0 && e / a.E_loc == d) coef += a.topk_weights[g * a.k + j];
-                    }
+            }
+            float coef = 1.0f;
+            if (a.weighted) {
+                coef = 0.0f;
+                for (int j = 0; j < a.k; ++j) {
+                    const int rj = __shfl_sync(0xFFFFFFFFu, rank_j, j);
+                    const float wj = __shfl_sync(0xFFFFFFFFu, w_j, j);
+                    if (rj == d) coef += wj;
                 }
             }
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
@@ -81,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
             a.combined_topk_weights[g * a.k + lane] = sum;
         }
 
-        gather_reduce_row<U>(a.y, s_row[warp], s_coef[warp], nd, a.H,
+        gather_reduce_row<U, P>(a.y, s_row[warp], s_coef[warp], nd, a.H,
                              a.out + g * (int64_t)a.H * 2, lane, 32);
         __syncwarp();
     }
@@ -132,12 +146,12 @@ extern "C" ep_status ep_combine(const ep_shape* sh, const void* y, const int64_t
         int64_t blocks = (ntok + kWarps - 1) / kWarps;
         if (sh->num_sms > 0) {
             int per_sm = 0;
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<2>, kThreads, 0);
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<kU, kP>, kThreads, 0);
             if (e != cudaSuccess) return cuda_fail(e);
             const int64_t cap = (int64_t)sh->num_sms * (per_sm > 0 ? per_sm : 1);
             if (blocks > cap) blocks = cap;
         }
-        cudaError_t e = launch_pdl(combine_kernel<2>, dim3((unsigned)blocks), dim3(kThreads), 0,
+        cudaError_t e = launch_pdl(combine_kernel<kU, kP>, dim3((unsigned)blocks), dim3(kThreads), 0,
                                    launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }

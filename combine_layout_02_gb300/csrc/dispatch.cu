@@ -186,7 +186,7 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)
         st = launch_dispatch<kQuant, 2>(a, sh->num_sms, launch->stream);
     else
-        st = launch_dispatch<kCopy, 4>(a, sh->num_sms, launch->stream);
+        st = launch_dispatch<kCopy, 8>(a, sh->num_sms, launch->stream);
     if (st != EP_OK) return st;
     return end_call(launch);
 }

@@ -24,8 +24,9 @@
 namespace ep {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+static_assert(EP_MAX_RANKS % kWarps == 0, "destinations split evenly over warps");
 
 struct LayoutArgs {
     const int64_t* topk_idx;
@@ -121,49 +122,81 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
 }
 
 __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
+    constexpr int kDPerWarp = EP_MAX_RANKS / kWarps;   // destinations per warp, at most
     __shared__ int s_base[EP_MAX_RANKS];
     __shared__ int s_warp_tot[kWarps][EP_MAX_RANKS];
     __shared__ int s_warp_off[kWarps][EP_MAX_RANKS];
     const int c = blockIdx.x, s = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = a.R, C = a.C, E = a.E;
+    const int nblocks = R * C, b = s * C + c;
+    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
     pdl_trigger();
     pdl_wait();
 
-    // (1) One warp per destination d: A = tokens of earlier sources, B = tokens of
+    // ---- Loads. Everything the block reads first is loaded before any store or
+    // barrier, so the loads share one memory round trip.
+    // Rank bits of this thread's token in the first tile.
+    const int t_first = t0 + threadIdx.x;
+    uint64_t mask = (t_first < t1) ? read_rank_bytes(a.in_rank + ((int64_t)s * a.T + t_first) * R, R) : 0ull;
+    // (1) Per destination d (warp-owned): A = tokens of earlier sources, B = tokens of
     // earlier channels of s, own = this channel, F = all channels of s.
-    for (int d = warp; d < R; d += kWarps) {
-        int A = 0, B = 0, own = 0, F = 0;
+    int A[kDPerWarp], B[kDPerWarp], own[kDPerWarp], F[kDPerWarp];
+#pragma unroll
+    for (int q = 0; q < kDPerWarp; ++q) {
+        A[q] = B[q] = own[q] = F[q] = 0;
+        const int d = warp + q * kWarps;
+        if (d < R) {
 #pragma unroll 4
-        for (int i = lane; i < s * C; i += 32) {
-            const int sp = i / C, cp = i - sp * C;
-            A += a.ws_cnt[((int64_t)sp * R + d) * C + cp];
-        }
-        for (int cp = lane; cp < C; cp += 32) {
-            const int v = a.ws_cnt[((int64_t)s * R + d) * C + cp];
-            F += v;
-            if (cp < c) B += v;
-            if (cp == c) own = v;
-        }
-        A = warp_sum(A);
-        B = warp_sum(B);
-        own = warp_sum(own);
-        F = warp_sum(F);
-        if (lane == 0) {
-            s_base[d] = A + B;
-            a.recv_channel_prefix[((int64_t)d * R + s) * C + c] = A + B;
-            a.channel_prefix[((int64_t)s * R + d) * C + c] = B + own;
-            if (c == 0) {
-                a.rank_prefix[s * R + d] = A + F;
-                if (a.num_tokens_per_rank != nullptr) a.num_tokens_per_rank[s * R + d] = F;
+            for (int i = lane; i < s * C; i += 32) {
+                const int sp = i / C, cp = i - sp * C;
+                A[q] += a.ws_cnt[((int64_t)sp * R + d) * C + cp];
+            }
+            for (int cp = lane; cp < C; cp += 32) {
+                const int v = a.ws_cnt[((int64_t)s * R + d) * C + cp];
+                F[q] += v;
+                if (cp < c) B[q] += v;
+                if (cp == c) own[q] += v;
             }
         }
     }
+    // (2) Per-source expert totals: one (source, expert) pair per thread of the grid.
+    const int p2 = b * kThreads + threadIdx.x;
+    int sum2 = 0;
+    if (a.num_tokens_per_expert != nullptr && p2 < R * E) {
+        const int sp = p2 / E, e = p2 - sp * E;
+#pragma unroll 4
+        for (int cp = 0; cp < C; ++cp) sum2 += a.ws_expert[((int64_t)sp * C + cp) * E + e];
+    }
+    // (3) Per-expert receive totals: one expert per warp of the grid.
+    const int e3 = b * kWarps + warp;
+    int sum3 = 0;
+    if (e3 < E) {
+#pragma unroll 4
+        for (int i = lane; i < R * C; i += 32) sum3 += a.ws_expert[(int64_t)i * E + e3];
+    }
 
-    // (2) Expert totals, spread over every block of the grid.
-    const int nblocks = R * C, b = s * C + c;
+    // ---- Reductions and stores.
+#pragma unroll
+    for (int q = 0; q < kDPerWarp; ++q) {
+        const int d = warp + q * kWarps;
+        if (d < R) {
+            const int Aq = warp_sum(A[q]), Bq = warp_sum(B[q]), oq = warp_sum(own[q]), Fq = warp_sum(F[q]);
+            if (lane == 0) {
+                s_base[d] = Aq + Bq;
+                a.recv_channel_prefix[((int64_t)d * R + s) * C + c] = Aq + Bq;
+                a.channel_prefix[((int64_t)s * R + d) * C + c] = Bq + oq;
+                if (c == 0) {
+                    a.rank_prefix[s * R + d] = Aq + Fq;
+                    if (a.num_tokens_per_rank != nullptr) a.num_tokens_per_rank[s * R + d] = Fq;
+                }
+            }
+        }
+    }
     if (a.num_tokens_per_expert != nullptr) {
-        for (int p = b * kThreads + threadIdx.x; p < R * E; p += nblocks * kThreads) {
+        if (p2 < R * E) a.num_tokens_per_expert[p2] = sum2;
+        // Grids smaller than R*E threads take the remaining pairs in further passes.
+        for (int p = p2 + nblocks * kThreads; p < R * E; p += nblocks * kThreads) {
             const int sp = p / E, e = p - sp * E;
             int sum = 0;
 #pragma unroll 4
@@ -171,20 +204,24 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
             a.num_tokens_per_expert[p] = sum;
         }
     }
-    for (int e = b * kWarps + warp; e < E; e += nblocks * kWarps) {
-        int sum = 0;
+    if (e3 < E) {
+        sum3 = warp_sum(sum3);
+        if (lane == 0) a.num_recv_per_expert[e3] = sum3;
+        for (int e = e3 + nblocks * kWarps; e < E; e += nblocks * kWarps) {
+            int sum = 0;
 #pragma unroll 4
-        for (int i = lane; i < R * C; i += 32) sum += a.ws_expert[(int64_t)i * E + e];
-        sum = warp_sum(sum);
-        if (lane == 0) a.num_recv_per_expert[e] = sum;
+            for (int i = lane; i < R * C; i += 32) sum += a.ws_expert[(int64_t)i * E + e];
+            sum = warp_sum(sum);
+            if (lane == 0) a.num_recv_per_expert[e] = sum;
+        }
     }
     __syncthreads();
 
-    // (3) send_head for the tokens of channel c of source s.
-    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
+    // ---- send_head for the tokens of channel c of source s (block-wide scan).
     for (int tile = t0; tile < t1; tile += kThreads) {   // block-uniform trip count
         const int t = tile + threadIdx.x;
-        const uint64_t mask = (t < t1) ? read_rank_bytes(a.in_rank + ((int64_t)s * a.T + t) * R, R) : 0ull;
+        if (tile != t0)
+            mask = (t < t1) ? read_rank_bytes(a.in_rank + ((int64_t)s * a.T + t) * R, R) : 0ull;
         for (int d = 0; d < R; ++d) {
             const unsigned bal = __ballot_sync(0xFFFFFFFFu, (mask >> d) & 1ull);
             if (lane == 0) s_warp_tot[warp][d] = __popc(bal);

@@ -25,6 +25,9 @@ namespace ep {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCombineU = 1;        // units per thread per batch in the LL combine
+
+__device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
 
 struct LLArgs {
     const char* x;
@@ -39,40 +42,77 @@ struct LLArgs {
     int32_t* layout_range;
     const char* y;
     char* out;
-    int R, T, H, E, k, E_loc, nmax, use_fp8;
+    int R, T, H, E, k, E_loc, nmax, use_fp8, write_recv;
+    int col_split;                  // combine: blocks per token (column ranges)
     uint32_t* err;
 };
 
-// Blocks [0, R*T): one per source token. Blocks [R*T, R*T + R): count signal of one
-// source rank.
+// Blocks [0, R*T): one per source token. Blocks [R*T, R*T + R): the count signals of
+// one destination rank d (sent by every source to d). When the receive phase runs in
+// the same launch (write_recv), those blocks also write recv_expert_count and
+// layout_range for d, since they already hold every count d receives.
 __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     __shared__ int64_t s_e[EP_MAX_TOPK];
     __shared__ int s_cnt[EP_MAX_TOPK];
     __shared__ int64_t s_rows[EP_MAX_TOPK];
     __shared__ int s_nv;
-    extern __shared__ int hist[];   // [E], count blocks only
+    extern __shared__ int hist[];   // [R][E_loc], count blocks only
     const int b = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
     pdl_wait();
 
     if (b >= a.R * a.T) {
-        const int s = b - a.R * a.T;
-        for (int e = threadIdx.x; e < a.E; e += kThreads) hist[e] = 0;
+        const int d = b - a.R * a.T;
+        const int lo = d * a.E_loc;
+        for (int i = threadIdx.x; i < a.E; i += kThreads) hist[i] = 0;
         __syncthreads();
-        const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
-        for (int i = threadIdx.x; i < a.T * a.k; i += kThreads) {
-            const int64_t e = tk[i];
-            if (e >= 0 && e < a.E) atomicAdd(&hist[(int)e], 1);
+        const int tk_per_src = a.T * a.k;
+#pragma unroll 8
+        for (int i = threadIdx.x; i < a.R * tk_per_src; i += kThreads) {
+            const int64_t e = __ldg(a.topk_idx + i);
+            if (e >= lo && e < lo + a.E_loc) atomicAdd(&hist[(i / tk_per_src) * a.E_loc + (int)(e - lo)], 1);
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < a.E; e += kThreads)
-            a.send_count[(int64_t)e * a.R + s] = min(hist[e], a.nmax);   // e = d*E_loc + el
+        for (int i = threadIdx.x; i < a.E; i += kThreads) {
+            const int s = i / a.E_loc, el = i - s * a.E_loc;
+            const int c = min(hist[i], a.nmax);
+            const int64_t sig = ((int64_t)(lo + el)) * a.R + s;       // [d][el][s]
+            a.send_count[sig] = c;
+            if (a.write_recv) {
+                a.layout_range[sig * 2 + 0] = s * a.nmax;
+                a.layout_range[sig * 2 + 1] = c;
+            }
+        }
+        if (a.write_recv) {
+            for (int el = threadIdx.x; el < a.E_loc; el += kThreads) {
+                int total = 0;
+                for (int s = 0; s < a.R; ++s) total += min(hist[s * a.E_loc + el], a.nmax);
+                a.recv_expert_count[lo + el] = total;
+            }
+        }
         pdl_trigger();
         return;
     }
 
     const int s = b / a.T, t = b - s * a.T;
     const int64_t tok = (int64_t)s * a.T + t;
+    const char* src = a.x + tok * (int64_t)a.H * 2;
+    // The token's row does not depend on the slot ranks: load its first batch now, so the
+    // load overlaps the rank scan below.
+    const int qunits = a.H >> 4;                 // fp8: 16 channels per unit
+    const int cunits = a.H >> 3;                 // bf16 copy: 8 channels per unit
+    uint4 pre[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        pre[i] = make_uint4(0, 0, 0, 0);
+        if (a.use_fp8) {
+            const int u = threadIdx.x + (i >> 1) * kThreads;
+            if (u < qunits) pre[i] = ld_stream_v4(src + (int64_t)u * 32 + (i & 1) * 16);
+        } else {
+            const int u = threadIdx.x + i * kThreads;
+            if (u < cunits) pre[i] = ld_stream_v4(src + (int64_t)u * 16);
+        }
+    }
     if (threadIdx.x < a.k) {
         s_e[threadIdx.x] = a.topk_idx[tok * a.k + threadIdx.x];
         s_cnt[threadIdx.x] = 0;
@@ -82,8 +122,9 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     // Rank of each entry among the source's earlier entries with the same expert.
     const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
     const int lim = t * a.k + a.k;
+#pragma unroll 4
     for (int i = threadIdx.x; i < lim; i += kThreads) {
-        const int64_t e = tk[i];
+        const int64_t e = __ldg(tk + i);
         if (e < 0) continue;
         for (int j = 0; j < a.k; ++j)
             if (e == s_e[j] && i < t * a.k + j) atomicAdd(&s_cnt[j], 1);
@@ -118,13 +159,33 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
         s_nv = n;
     }
     __syncthreads();
+    const int nv = s_nv;
 
-    const char* src = a.x + tok * (int64_t)a.H * 2;
-    if (a.use_fp8)
-        scatter_quant_row<1>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales, s_rows, s_nv,
-                             a.H, threadIdx.x, kThreads);
-    else
-        scatter_copy_row<2>(src, a.recv_x, s_rows, s_nv, (int64_t)a.H * 2, threadIdx.x, kThreads);
+    if (a.use_fp8) {
+        uint8_t* q_base = reinterpret_cast<uint8_t*>(a.recv_x);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {            // the prefetched units (all lanes shuffle)
+            const int u = threadIdx.x + i * kThreads;
+            float scale;
+            const uint4 q = quant_unit(pre[2 * i], pre[2 * i + 1], scale);
+            if (u < qunits) store_quant_unit(q_base, a.recv_x_scales, s_rows, nv, a.H, u, q, scale);
+        }
+        scatter_quant_row<1>(src, q_base, a.recv_x_scales, s_rows, nv, a.H, threadIdx.x, kThreads,
+                             2 * kThreads);
+    } else {
+        for (int p = 0; p < nv; ++p) {
+            char* dst = a.recv_x + s_rows[p] * (int64_t)a.H * 2;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int u = threadIdx.x + i * kThreads;
+                if (u < cunits) st_v4(dst + (int64_t)u * 16, pre[i]);
+            }
+        }
+        for (int u = threadIdx.x + 4 * kThreads; u < cunits; u += kThreads) {
+            const uint4 v = ld_stream_v4(src + (int64_t)u * 16);
+            for (int p = 0; p < nv; ++p) st_v4(a.recv_x + s_rows[p] * (int64_t)a.H * 2 + (int64_t)u * 16, v);
+        }
+    }
     pdl_trigger();
 }
 
@@ -145,6 +206,8 @@ __global__ void __launch_bounds__(kThreads) ll_recv_kernel(LLArgs a) {
 }
 
 // One block per output token: weighted sum over the token's valid entries.
+// Block (token, column part): blockIdx.y selects a contiguous range of 16-byte units so
+// that each thread's loads for the part are issued in one batch.
 __global__ void __launch_bounds__(kThreads) ll_combine_kernel(LLArgs a) {
     __shared__ int64_t s_rows[EP_MAX_TOPK];
     __shared__ float s_w[EP_MAX_TOPK];
@@ -176,7 +239,11 @@ __global__ void __launch_bounds__(kThreads) ll_combine_kernel(LLArgs a) {
         s_nv = n;
     }
     __syncthreads();
-    gather_reduce_row<1>(a.y, s_rows, s_w, s_nv, a.H, a.out + tok * (int64_t)a.H * 2, threadIdx.x, kThreads);
+    const int units = a.H >> 3;
+    const int per = ceil_div_dev(units, a.col_split);
+    const int u_begin = blockIdx.y * per;
+    gather_reduce_row<kCombineU>(a.y, s_rows, s_w, s_nv, a.H, a.out + tok * (int64_t)a.H * 2,
+                                 threadIdx.x, kThreads, u_begin, min(units, u_begin + per));
     pdl_trigger();
 }
 
@@ -232,6 +299,7 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     a.E_loc = a.E / a.R;
     a.nmax = sh->num_max_dispatch_tokens_per_rank;
     a.use_fp8 = use_fp8 ? 1 : 0;
+    a.write_recv = (phase & EP_PHASE_RECV) ? 1 : 0;
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;
@@ -241,7 +309,10 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
                                    sizeof(int) * (size_t)a.E, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }
-    if (phase & EP_PHASE_RECV) {
+    if (phase == EP_PHASE_RECV) {
+        // Receive phase launched on its own (the hook): turn the count signals written
+        // by the send phase into counts and layout ranges. With EP_PHASE_BOTH the send
+        // kernel's count blocks already wrote them.
         cudaError_t e = launch_pdl(ll_recv_kernel, dim3((unsigned)ceil_div(a.E, kThreads)),
                                    dim3(kThreads), 0, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
@@ -281,8 +352,9 @@ ep_status ep_ll_combine(const ep_shape* sh, const void* y, const int64_t* topk_i
     // Send phase: in one device memory the return transfer is nothing; the call only
     // orders the stream (wait_event) and records the completion event.
     if ((phase & EP_PHASE_RECV) && a.R * a.T > 0) {
-        cudaError_t e = launch_pdl(ll_combine_kernel, dim3((unsigned)(a.R * a.T)), dim3(kThreads), 0,
-                                   launch->stream, a);
+        a.col_split = 1;
+        cudaError_t e = launch_pdl(ll_combine_kernel, dim3((unsigned)(a.R * a.T), (unsigned)a.col_split),
+                                   dim3(kThreads), 0, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);

@@ -15,7 +15,7 @@
 
 namespace ep {
 
-template <int U>
+template <int U, bool kStreamStore = false>
 __device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
                                                  char* __restrict__ dst_base,
                                                  const int64_t* rows, int nd, int64_t row_bytes,
@@ -33,7 +33,10 @@ __device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
 #pragma unroll
             for (int i = 0; i < U; ++i) {
                 const int u = u0 + i * stride + first;
-                if (u < units) st_v4(dst + (int64_t)u * 16, v[i]);
+                if (u < units) {
+                    if (kStreamStore) st_stream_v4(dst + (int64_t)u * 16, v[i]);
+                    else st_v4(dst + (int64_t)u * 16, v[i]);
+                }
             }
         }
     }
@@ -47,15 +50,55 @@ __device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
 // must call this (the shuffles use the full mask).
 //   amax' = max(amax, 1e-4), scale = amax' / 448 (IEEE division),
 //   inv = 448 / amax' (IEEE division), q = e4m3_rn_satfinite(x * inv).
+// Quantises one unit (16 bf16 channels held in a, b) to 16 e4m3 bytes and returns the
+// group scale. Must be called by all 32 lanes of the warp together (8-lane shuffles).
+__device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, float& scale) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    float f[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        f[2 * j] = bf16_lo(w[j]);
+        f[2 * j + 1] = bf16_hi(w[j]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    const float am = fmaxf(amax, 1e-4f);
+    scale = __fdiv_rn(am, 448.0f);
+    const float inv = __fdiv_rn(448.0f, am);
+    uint32_t qw[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
+        const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
+        qw[j] = lo | (hi << 16);
+    }
+    return make_uint4(qw[0], qw[1], qw[2], qw[3]);
+}
+
+// Stores one quantised unit u (and, for the first unit of a group, its scale) to every
+// destination row.
+__device__ __forceinline__ void store_quant_unit(uint8_t* __restrict__ q_base, float* __restrict__ s_base,
+                                                 const int64_t* rows, int nd, int H, int u,
+                                                 const uint4& q, float scale) {
+    const int G = H >> 7;
+    for (int p = 0; p < nd; ++p) {
+        st_v4(q_base + rows[p] * (int64_t)H + (int64_t)u * 16, q);
+        if ((u & 7) == 0) s_base[rows[p] * (int64_t)G + (u >> 3)] = scale;
+    }
+}
+
 template <int U>
 __device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
                                                   uint8_t* __restrict__ q_base,
                                                   float* __restrict__ s_base,
                                                   const int64_t* rows, int nd, int H,
-                                                  int first, int stride) {
+                                                  int first, int stride, int u_start = 0) {
     const int units = H >> 4;
-    const int G = H >> 7;
-    for (int u0 = 0; u0 < units; u0 += stride * U) {
+    for (int u0 = u_start; u0 < units; u0 += stride * U) {
         uint4 a[U], b[U];
 #pragma unroll
         for (int i = 0; i < U; ++i) {
@@ -71,53 +114,26 @@ __device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
 #pragma unroll
         for (int i = 0; i < U; ++i) {
             const int u = u0 + i * stride + first;
-            const uint32_t w[8] = {a[i].x, a[i].y, a[i].z, a[i].w, b[i].x, b[i].y, b[i].z, b[i].w};
-            float f[16];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                f[2 * j] = bf16_lo(w[j]);
-                f[2 * j + 1] = bf16_hi(w[j]);
-            }
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-            const float am = fmaxf(amax, 1e-4f);
-            const float scale = __fdiv_rn(am, 448.0f);
-            const float inv = __fdiv_rn(448.0f, am);
-            uint4 q;
-            uint32_t qw[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
-                const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
-                qw[j] = lo | (hi << 16);
-            }
-            q = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-            if (u < units) {
-                for (int p = 0; p < nd; ++p) {
-                    st_v4(q_base + rows[p] * (int64_t)H + (int64_t)u * 16, q);
-                    if ((u & 7) == 0) s_base[rows[p] * (int64_t)G + (u >> 3)] = scale;
-                }
-            }
+            float scale;
+            const uint4 q = quant_unit(a[i], b[i], scale);
+            if (u < units) store_quant_unit(q_base, s_base, rows, nd, H, u, q, scale);
         }
     }
 }
 
 // out = sum_p coef[p] * rows[p], fp32 accumulation in registers, one bf16 RNE store.
-// Unit = 8 channels (16 bytes). Rows are taken 8 at a time with every load of the
-// batch issued before the first accumulation.
-template <int U>
+// Unit = 8 channels (16 bytes); units [u_begin, u_end) of the row. Rows are taken P at a
+// time with every load of the batch (P rows x U units) issued before the first
+// accumulation.
+template <int U, int P = 8>
 __device__ __forceinline__ void gather_reduce_row(const char* __restrict__ y_base,
                                                   const int64_t* rows, const float* coef,
                                                   int nd, int H, char* __restrict__ out_row,
-                                                  int first, int stride) {
-    constexpr int P = 8;
-    const int units = H >> 3;
+                                                  int first, int stride, int u_begin = 0,
+                                                  int u_end = 1 << 30) {
+    const int units = min(H >> 3, u_end);
     const int64_t row_bytes = (int64_t)H * 2;
-    for (int u0 = 0; u0 < units; u0 += stride * U) {
+    for (int u0 = u_begin; u0 < units; u0 += stride * U) {
         float acc[U][8];
 #pragma unroll
         for (int i = 0; i < U; ++i)
