@@ -300,6 +300,8 @@ def make_plan(args, ep, dev, stream, launch):
                           launch)
 
         dname = "dispatch_fp8" if fp8 else "dispatch"
+        # The plan owns every buffer whose raw pointers the calls use.
+        plan["keep"] = (lb, rb, y, out, xs)
         plan["phases"] = ([] if reuse else [("layout", layout)]) + [(dname, dispatch), ("combine", combine)]
         plan["out"] = out
 
@@ -323,6 +325,9 @@ def make_plan(args, ep, dev, stream, launch):
         ep.ep_ll_dispatch(sh, x, topk, False, ep.EP_PHASE_BOTH, ybuf.struct(), launch)
         out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
         s_buf, s_y = buf.struct(), ybuf.struct()
+        # The plan owns every buffer whose raw pointers the calls use (s_buf / s_y hold
+        # only addresses; without this, buf's memory would be freed after this function).
+        plan["keep"] = (buf, ybuf, out)
         plan["phases"] = [
             ("ll_send", lambda: ep.ep_ll_dispatch(sh, x, topk, True, ep.EP_PHASE_SEND, s_buf, launch)),
             ("ll_recv", lambda: ep.ep_ll_dispatch(sh, x, topk, True, ep.EP_PHASE_RECV, s_buf, launch)),
@@ -342,6 +347,48 @@ def make_plan(args, ep, dev, stream, launch):
     else:
         raise ValueError(args.workload)
     return plan
+
+
+def run_graph(args, world, dev, launch, step, flush_buf, total_bytes):
+    """The same step captured once as a CUDA graph and replayed K times (whole-step time;
+    with a flush, each replay is timed alone after the flush)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    saved = launch.stream
+    try:
+        with torch.cuda.graph(g, stream=s):
+            launch.stream = torch.cuda.current_stream().cuda_stream
+            step()
+    finally:
+        launch.stream = saved
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    n = args.steps
+    if flush_buf is None:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / n
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush_buf.zero_()
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    ms = reduce_max(ms, world, dev)
+    return {"ms_per_step": round(ms, 4), "value": round(world * total_bytes / (ms * 1e6), 1),
+            "unit": "GB/s"}
 
 
 def run_ours(args, rank, world):
@@ -412,6 +459,10 @@ def run_ours(args, rank, world):
     if flags != 0:
         raise RuntimeError(f"device error flags set: {flags}")
 
+    graph = None if args.no_graph else run_graph(args, world, dev, launch, step, flush_buf, total_bytes)
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error flags set: {int(err.item())}")
+
     e2e = None
     if args.workload == "dsv3" and not args.no_e2e:
         e2e = run_e2e(world, dev, stream, step, plan["x"], plan["topk"], plan["wts"], plan["out"],
@@ -458,6 +509,7 @@ def run_ours(args, rank, world):
                           "traffic": traffic_from_profiles(PHASE_KERNEL[dom]),
                           "algorithmic_bytes_per_launch": nbytes[dom]}
     result["e2e"] = e2e
+    result["graph"] = graph
     result["gpu_launches"] = launches
     result["clocks"] = clocks
     result["clocks_remeasured"] = remeasured
@@ -531,6 +583,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="dsv3",
                     help="dsv3 is the benchmark line; the others are extra measurements")
     ap.add_argument("--nmax", type=int, default=0,
