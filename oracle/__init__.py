@@ -31,14 +31,16 @@ def lib():
         L.oracle_bf16_from_double.argtypes = [P, I64, P]
         L.oracle_e4m3_encode.argtypes = [P, I64, P]
         L.oracle_e4m3_decode.argtypes = [P, I64, P]
+        F = ctypes.c_float
         L.oracle_quantize_row.argtypes = [P, I, P, P]
+        L.oracle_quantize_row_mode.argtypes = [P, I, I, F, P, P, P]
         L.oracle_layout.argtypes = [I, I, I, I, I, P, P, P, P, P, P, P, P, P]
         L.oracle_layout.restype = I64
-        L.oracle_dispatch.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P, P, P, P]
+        L.oracle_dispatch.argtypes = [I, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P]
         L.oracle_dispatch.restype = I64
         L.oracle_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P]
         L.oracle_combine.restype = I64
-        L.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P, P]
+        L.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P]
         L.oracle_ll_dispatch.restype = I64
         L.oracle_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P]
         L.oracle_ll_combine.restype = None
@@ -80,16 +82,22 @@ def e4m3_decode(b) -> np.ndarray:
     return out
 
 
-def quantize_rows(x: np.ndarray):
-    """x: [..., H] bf16 bits -> (q [..., H] uint8, scales [..., H/128] fp32)."""
+SCALE_FP32, SCALE_POW2, SCALE_UE8M0, SCALE_TENSOR = 0, 1, 2, 3
+
+
+def quantize_rows(x: np.ndarray, scale_mode: int = SCALE_FP32, tensor_scale: float = 0.0):
+    """x: [..., H] bf16 bits -> (q [..., H] uint8, scales [..., H/128]); scales are fp32,
+    or uint8 biased exponents in the UE8M0 mode."""
     x = np.ascontiguousarray(x, dtype=np.uint16)
     H = x.shape[-1]
     rows = x.reshape(-1, H)
     q = np.empty(rows.shape, dtype=np.uint8)
-    sc = np.empty((rows.shape[0], H // 128), dtype=np.float32)
+    ue = scale_mode == SCALE_UE8M0
+    sc = np.empty((rows.shape[0], H // 128), dtype=np.uint8 if ue else np.float32)
     L = lib()
     for i in range(rows.shape[0]):
-        L.oracle_quantize_row(_p(rows[i]), H, _p(q[i]), _p(sc[i]))
+        L.oracle_quantize_row_mode(_p(rows[i]), H, scale_mode, tensor_scale, _p(q[i]),
+                                   None if ue else _p(sc[i]), _p(sc[i]) if ue else None)
     return q.reshape(x.shape), sc.reshape(x.shape[:-1] + (H // 128,))
 
 
@@ -128,7 +136,8 @@ X_BF16, X_QUANTIZE, X_FP8 = 0, 1, 2
 def dispatch(x: np.ndarray, send_head: np.ndarray, row_offset: np.ndarray, E: int,
              topk_idx: Optional[np.ndarray] = None, topk_weights: Optional[np.ndarray] = None,
              x_kind: int = X_BF16, x_scales: Optional[np.ndarray] = None,
-             fill_x: int = 0, fill_idx: int = 0, fill_w: float = 0.0, fill_src: int = 0) -> dict:
+             fill_x: int = 0, fill_idx: int = 0, fill_w: float = 0.0, fill_src: int = 0,
+             scale_mode: int = SCALE_FP32, tensor_scale: float = 0.0) -> dict:
     """Normal dispatch. x [R, T, H] (uint16 bf16 bits, or uint8 e4m3 when x_kind=2).
 
     Output arrays are created with the given fill values, so rows that no token maps
@@ -142,8 +151,12 @@ def dispatch(x: np.ndarray, send_head: np.ndarray, row_offset: np.ndarray, E: in
     out_dtype = np.uint16 if x_kind == X_BF16 else np.uint8
     res = {"recv_x": np.full((rows, H), fill_x, out_dtype),
            "recv_src_idx": np.full((rows,), fill_src, np.int32)}
-    res["recv_x_scales"] = (np.full((rows, H // 128), np.nan, np.float32)
-                            if x_kind != X_BF16 else None)
+    if x_kind == X_BF16:
+        res["recv_x_scales"] = None
+    elif x_kind == X_QUANTIZE and scale_mode == SCALE_UE8M0:
+        res["recv_x_scales"] = np.full((rows, H // 128), 0xEE, np.uint8)
+    else:
+        res["recv_x_scales"] = np.full((rows, H // 128), np.nan, np.float32)
     if topk_idx is not None:
         res["recv_topk_idx"] = np.full((rows, k), fill_idx, np.int64)
         res["recv_topk_weights"] = (np.full((rows, k), fill_w, np.float32)
@@ -152,7 +165,7 @@ def dispatch(x: np.ndarray, send_head: np.ndarray, row_offset: np.ndarray, E: in
         res["recv_topk_idx"] = res["recv_topk_weights"] = None
     x = np.ascontiguousarray(x)
     bad = lib().oracle_dispatch(
-        R, T, H, E, k, x_kind, _p(x), _p(_c(x_scales, np.float32)),
+        R, T, H, E, k, x_kind, scale_mode, tensor_scale, _p(x), _p(_c(x_scales, np.float32)),
         _p(_c(topk_idx, np.int64)), _p(_c(topk_weights, np.float32)),
         _p(send_head), _p(row_offset), _p(res["recv_x"]), _p(res["recv_x_scales"]),
         _p(res["recv_topk_idx"]), _p(res["recv_topk_weights"]), _p(res["recv_src_idx"]))
@@ -187,7 +200,8 @@ def combine(y: np.ndarray, send_head: np.ndarray, row_offset: np.ndarray, E: int
 # ---------------------------------------------------------------- low latency
 
 def ll_dispatch(x: np.ndarray, topk_idx: np.ndarray, E: int, nmax: int, use_fp8: bool,
-                fill_x: int = 0, fill_src: int = -7) -> dict:
+                fill_x: int = 0, fill_src: int = -7, scale_mode: int = SCALE_FP32,
+                tensor_scale: float = 0.0) -> dict:
     """Low-latency dispatch into fixed per-(expert, source) slots."""
     x = _c(x, np.uint16)
     topk_idx = _c(topk_idx, np.int64)
@@ -197,15 +211,18 @@ def ll_dispatch(x: np.ndarray, topk_idx: np.ndarray, E: int, nmax: int, use_fp8:
     slots = R * nmax
     res = {
         "recv_x": np.full((R, E_loc, slots, H), fill_x, np.uint8 if use_fp8 else np.uint16),
-        "recv_x_scales": (np.full((R, E_loc, slots, H // 128), np.nan, np.float32)
-                          if use_fp8 else None),
+        "recv_x_scales": (None if not use_fp8 else
+                          np.full((R, E_loc, slots, H // 128), 0xEE, np.uint8)
+                          if scale_mode == SCALE_UE8M0 else
+                          np.full((R, E_loc, slots, H // 128), np.nan, np.float32)),
         "src_info": np.full((R, E_loc, slots), fill_src, np.int32),
         "slot": np.empty((R, T, k), np.int32),
         "recv_expert_count": np.empty((R, E_loc), np.int32),
         "layout_range": np.empty((R, E_loc, R, 2), np.int32),
     }
     bad = lib().oracle_ll_dispatch(
-        R, T, H, E, k, nmax, int(bool(use_fp8)), _p(x), _p(topk_idx), _p(res["recv_x"]),
+        R, T, H, E, k, nmax, int(bool(use_fp8)), scale_mode, tensor_scale, _p(x), _p(topk_idx),
+        _p(res["recv_x"]),
         _p(res["recv_x_scales"]), _p(res["src_info"]), _p(res["slot"]),
         _p(res["recv_expert_count"]), _p(res["layout_range"]))
     res["bad_entries"] = int(bad)

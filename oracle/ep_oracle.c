@@ -146,13 +146,31 @@ EXPORT void oracle_e4m3_decode(const uint8_t* b, int64_t n, double* out)
 /* ------------------------------------------------------------------------- */
 
 /*
- * [README] feature notes: FP8 dispatch with per-group scales. Group = 128 channels.
- * Per group g: amax = max |x|; amax' = max(amax, 1e-4) (floor for all-zero groups,
- * a choice of this project); scale = amax' / 448; inv = 448 / amax'; q = e4m3(x * inv)
- * with one fp32 multiply. All float operations are single IEEE fp32 operations.
- * Reading: "scale" is the dequantisation factor, x ~= e4m3_value(q) * scale.
+ * [README] feature notes: FP8 dispatch with per-group scales, and the two scale modes
+ * round_scale (power-of-two scales) and use_ue8m0 (UE8M0 scale format), and a single
+ * per-tensor scale fp8_quant_scale. Group = 128 channels. Per group g:
+ *   amax = max |x|; amax' = max(amax, 1e-4) (floor for all-zero groups, a choice of
+ *   this project); s0 = amax' / 448 (one IEEE fp32 division).
+ *   mode 0 (fp32 scale):      scale = s0,                      inv = 448 / amax'
+ *   mode 1 (power of two):    scale = 2^ceil(log2(s0)),        inv = 1 / scale (exact)
+ *   mode 2 (UE8M0):           as mode 1; the scale is stored as the byte log2(scale) + 127
+ *   mode 3 (per tensor):      scale = the caller's s for every group, inv = 1 / s (fp32)
+ *   q = e4m3(x * inv), one fp32 multiply, round to nearest even, saturating.
+ * Readings: "scale" is the dequantisation factor (x ~= value(q) * scale); rounding the
+ * scale up to a power of two keeps |x * inv| <= 448; UE8M0 = unsigned 8-bit exponent
+ * with bias 127, no mantissa; a per-tensor scale is written to every group's slot so the
+ * receive format does not change.
+ * Scales go to scales_f32[g] (modes 0, 1, 3) or scales_u8[g] (mode 2).
  */
-EXPORT void oracle_quantize_row(const uint16_t* xrow, int H, uint8_t* q, float* scales)
+static float pow2_ceil(float v)
+{
+    int e;
+    double m = frexp((double)v, &e);     /* v = m * 2^e, 0.5 <= m < 1 */
+    return (float)ldexp(1.0, m == 0.5 ? e - 1 : e);
+}
+
+EXPORT void oracle_quantize_row_mode(const uint16_t* xrow, int H, int mode, float tensor_scale,
+                                     uint8_t* q, float* scales_f32, uint8_t* scales_u8)
 {
     for (int g = 0; g < H / 128; g++) {
         float amax = 0.0f;
@@ -161,14 +179,34 @@ EXPORT void oracle_quantize_row(const uint16_t* xrow, int H, uint8_t* q, float* 
             if (a > amax) amax = a;
         }
         float am = amax > 1e-4f ? amax : 1e-4f;
-        float scale = am / 448.0f;
-        float inv = 448.0f / am;
+        float scale, inv;
+        if (mode == 0) {
+            scale = am / 448.0f;
+            inv = 448.0f / am;
+        } else if (mode == 1 || mode == 2) {
+            scale = pow2_ceil(am / 448.0f);
+            inv = (float)(1.0 / (double)scale);          /* exact: scale is 2^n */
+        } else {
+            scale = tensor_scale;
+            inv = 1.0f / tensor_scale;
+        }
         for (int i = 0; i < 128; i++) {
             float v = bf16_bits_to_float(xrow[g * 128 + i]) * inv;
             q[g * 128 + i] = float_to_e4m3_rne_sat(v);
         }
-        scales[g] = scale;
+        if (mode == 2) {
+            int e;
+            (void)frexp((double)scale, &e);              /* scale = 2^(e-1) */
+            scales_u8[g] = (uint8_t)(e - 1 + 127);
+        } else {
+            scales_f32[g] = scale;
+        }
     }
+}
+
+EXPORT void oracle_quantize_row(const uint16_t* xrow, int H, uint8_t* q, float* scales)
+{
+    oracle_quantize_row_mode(xrow, H, 0, 0.0f, q, scales, NULL);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -294,16 +332,19 @@ EXPORT int64_t oracle_layout(int R, int T, int E, int k, int C, const int64_t* t
  * x_kind: 0 = bf16 rows copied as bf16 (elem 2 bytes);
  *         1 = bf16 rows quantised to e4m3 with per-128-channel scales;
  *         2 = pre-quantised e4m3 rows (x_scales [R][T][H/128]) copied byte for byte.
+ * scale_mode / tensor_scale: the quantisation mode of x_kind 1 (see above); in mode 2
+ * recv_x_scales holds one byte per group, otherwise one fp32 per group.
  * recv_topk_idx[row][j] = e - d*E_loc if e lives on d, else -1 (reading);
  * recv_topk_weights[row][j] = w if e lives on d, else 0 (reading);
  * recv_src_idx[row] = t. topk_idx == NULL (handle reuse) leaves the topk outputs alone.
  * Returns the number of rows that fell outside their region (skipped).
  */
 EXPORT int64_t oracle_dispatch(int R, int T, int H, int E, int k, int x_kind,
+                               int scale_mode, float tensor_scale,
                                const void* x, const float* x_scales,
                                const int64_t* topk_idx, const float* topk_weights,
                                const int32_t* send_head, const int64_t* row_offset,
-                               void* recv_x, float* recv_x_scales,
+                               void* recv_x, void* recv_x_scales,
                                int64_t* recv_topk_idx, float* recv_topk_weights,
                                int32_t* recv_src_idx)
 {
@@ -311,20 +352,23 @@ EXPORT int64_t oracle_dispatch(int R, int T, int H, int E, int k, int x_kind,
     const int G = H / 128;
     const size_t out_elem = (x_kind == 0) ? 2 : 1;
     int64_t bad = 0;
+    const size_t scale_elem = (x_kind == 1 && scale_mode == 2) ? 1 : 4;
     uint8_t* qrow = (uint8_t*)malloc((size_t)H + 1);
     float* srow = (float*)malloc(sizeof(float) * (size_t)(G + 1));
+    uint8_t* brow = (uint8_t*)malloc((size_t)G + 1);
 
     for (int s = 0; s < R; s++)
         for (int t = 0; t < T; t++) {
             const int64_t tok = (int64_t)s * T + t;
             const void* src_row;
-            const float* src_scales = NULL;
+            const void* src_scales = NULL;
             if (x_kind == 0) {
                 src_row = (const uint16_t*)x + tok * H;
             } else if (x_kind == 1) {
-                oracle_quantize_row((const uint16_t*)x + tok * H, H, qrow, srow);
+                oracle_quantize_row_mode((const uint16_t*)x + tok * H, H, scale_mode, tensor_scale,
+                                         qrow, srow, brow);
                 src_row = qrow;
-                src_scales = srow;
+                src_scales = scale_mode == 2 ? (const void*)brow : (const void*)srow;
             } else {
                 src_row = (const uint8_t*)x + tok * H;
                 src_scales = x_scales + tok * G;
@@ -336,7 +380,8 @@ EXPORT int64_t oracle_dispatch(int R, int T, int H, int E, int k, int x_kind,
                 if (row >= row_offset[d + 1]) { bad++; continue; }
                 memcpy((uint8_t*)recv_x + (size_t)row * H * out_elem, src_row, (size_t)H * out_elem);
                 if (x_kind != 0)
-                    memcpy(recv_x_scales + (size_t)row * G, src_scales, sizeof(float) * (size_t)G);
+                    memcpy((uint8_t*)recv_x_scales + (size_t)row * G * scale_elem, src_scales,
+                           scale_elem * (size_t)G);
                 if (recv_src_idx) recv_src_idx[row] = t;
                 if (topk_idx) {
                     for (int j = 0; j < k; j++) {
@@ -351,6 +396,7 @@ EXPORT int64_t oracle_dispatch(int R, int T, int H, int E, int k, int x_kind,
         }
     free(qrow);
     free(srow);
+    free(brow);
     return bad;
 }
 
@@ -427,14 +473,16 @@ EXPORT int64_t oracle_combine(int R, int T, int H, int E, int k, int mode,
  * expert e lands at pos = s*nmax + #{t' < t of source s that picked e}.
  *
  * Outputs: recv_x[d][el][pos] (bf16 copy, or e4m3 + per-128-channel scales when
- * use_fp8), src_info[d][el][pos] = t, slot[s][t][j] = pos (-1 when masked),
+ * use_fp8, quantised with scale_mode / tensor_scale as in oracle_quantize_row_mode;
+ * the port notes the UE8M0 format for these kernels), src_info[d][el][pos] = t, slot[s][t][j] = pos (-1 when masked),
  * recv_expert_count[d][el] = sum_s count, layout_range[d][el][s] = (s*nmax, count).
  * Counts are int32 (the port returns int32 counts and handles).
  * Returns the number of entries skipped (outside [0, E), or beyond nmax).
  */
 EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, int use_fp8,
+                                  int scale_mode, float tensor_scale,
                                   const uint16_t* x, const int64_t* topk_idx,
-                                  void* recv_x, float* recv_x_scales, int32_t* src_info,
+                                  void* recv_x, void* recv_x_scales, int32_t* src_info,
                                   int32_t* slot, int32_t* recv_expert_count,
                                   int32_t* layout_range)
 {
@@ -442,10 +490,12 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
     const int G = H / 128;
     const int64_t slots = (int64_t)R * nmax;
     const size_t out_elem = use_fp8 ? 1 : 2;
+    const size_t scale_elem = scale_mode == 2 ? 1 : 4;
     int64_t bad = 0;
     int32_t* run = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
     uint8_t* qrow = (uint8_t*)malloc((size_t)H + 1);
     float* srow = (float*)malloc(sizeof(float) * (size_t)(G + 1));
+    uint8_t* brow = (uint8_t*)malloc((size_t)G + 1);
 
     memset(recv_expert_count, 0, sizeof(int32_t) * (size_t)E);
     for (int s = 0; s < R; s++) {
@@ -453,7 +503,7 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
         for (int t = 0; t < T; t++) {
             const int64_t tok = (int64_t)s * T + t;
             const uint16_t* xrow = x + tok * H;
-            if (use_fp8) oracle_quantize_row(xrow, H, qrow, srow);
+            if (use_fp8) oracle_quantize_row_mode(xrow, H, scale_mode, tensor_scale, qrow, srow, brow);
             for (int j = 0; j < k; j++) {
                 int64_t e = topk_idx[tok * k + j];
                 slot[tok * k + j] = -1;
@@ -465,7 +515,8 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
                 int64_t dst = ((int64_t)d * E_loc + el) * slots + pos;
                 if (use_fp8) {
                     memcpy((uint8_t*)recv_x + (size_t)dst * H, qrow, (size_t)H);
-                    memcpy(recv_x_scales + (size_t)dst * G, srow, sizeof(float) * (size_t)G);
+                    memcpy((uint8_t*)recv_x_scales + (size_t)dst * G * scale_elem,
+                           scale_mode == 2 ? (const void*)brow : (const void*)srow, scale_elem * (size_t)G);
                 } else {
                     memcpy((uint8_t*)recv_x + (size_t)dst * H * out_elem, xrow, (size_t)H * out_elem);
                 }
@@ -484,6 +535,7 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
     free(run);
     free(qrow);
     free(srow);
+    free(brow);
     return bad;
 }
 

@@ -202,3 +202,78 @@ def test_quantize_hand_example():
     np.testing.assert_array_equal(q[0], expect)
     assert sc[0, 0] == np.float32(g["group0_amax"]) / np.float32(448.0)
     assert sc[0, 1] == np.float32(g["group1_amax_floor"]) / np.float32(448.0)
+
+
+# ----------------------------------------------------------------------------- scale modes
+
+def _torch_quantize_modes(xbits, mode, tensor_scale=0.0):
+    """Power-of-two / per-tensor quantisation through PyTorch ops: fp32 division, exact
+    power-of-two rounding via frexp, library e4m3 cast after clamping."""
+    x = torch.from_numpy(xbits.view(np.int16)).view(torch.bfloat16).float()
+    g = x.reshape(*x.shape[:-1], -1, 128)
+    if mode == oracle.SCALE_TENSOR:
+        s = torch.tensor(tensor_scale, dtype=torch.float32)
+        inv = torch.tensor(1.0, dtype=torch.float32) / s
+        scale = s.expand(g.shape[:-1])
+    else:
+        am = torch.clamp(g.abs().amax(dim=-1, keepdim=True), min=torch.tensor(1e-4))
+        s0 = am / 448.0
+        m, e = torch.frexp(s0)
+        scale = torch.ldexp(torch.ones_like(s0), torch.where(m == 0.5, e - 1, e))
+        inv = 1.0 / scale
+        scale = scale.squeeze(-1)
+    q = torch.clamp(g * inv, -448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return q.reshape(x.shape).numpy(), scale.numpy()
+
+
+@pytest.mark.parametrize("mode", [1, 2, 3])
+def test_scale_modes_match_torch_path(mode):
+    rng = np.random.default_rng(8)
+    x32 = (rng.standard_normal((48, 1024)) * np.exp2(rng.integers(-10, 10, (48, 1)))).astype(np.float32)
+    x32[0, :128] = 0.0
+    xb = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ts = 0.0173 if mode == 3 else 0.0
+    q, sc = oracle.quantize_rows(xb, mode, ts)
+    q_ref, sc_ref = _torch_quantize_modes(xb, mode, ts)
+    np.testing.assert_array_equal(q, q_ref)
+    if mode == 2:
+        # one byte per group: the biased exponent of the power-of-two scale
+        np.testing.assert_array_equal(sc.astype(np.float64), np.log2(sc_ref.astype(np.float64)) + 127)
+        q1, _ = oracle.quantize_rows(xb, 1)
+        np.testing.assert_array_equal(q, q1)           # same codes as the fp32 power-of-two mode
+    else:
+        np.testing.assert_array_equal(sc.view(np.uint32), sc_ref.astype(np.float32).view(np.uint32))
+    if mode in (1, 2):
+        s_f = np.exp2(sc.astype(np.float64) - 127) if mode == 2 else sc.astype(np.float64)
+        m, _ = np.frexp(s_f)
+        assert np.all(m == 0.5)                           # exact powers of two
+        amax = np.abs(_bf16_value(xb).reshape(48, 8, 128)).max(-1)
+        s0 = np.maximum(amax, np.float32(1e-4)).astype(np.float32) / np.float32(448)
+        assert np.all(s_f >= s0) and np.all(s_f / 2 < s0)  # the next power of two up
+
+
+def test_scale_modes_hand_example():
+    with open(os.path.join(GOLDEN, "fp8_scale_modes_hand_example.json")) as f:
+        g = json.load(f)
+    H = g["H"]
+    x = np.zeros((1, H), np.uint16)
+    for i, b in g["group0_values_bf16_bits"].items():
+        x[0, int(i)] = int(b, 16)
+    for mode in (1, 2):
+        q, sc = oracle.quantize_rows(x, mode)
+        exp = np.zeros(H, np.uint8)
+        for i, c in g["pow2_codes"].items():
+            exp[int(i)] = int(c, 16)
+        np.testing.assert_array_equal(q[0], exp)
+        if mode == 1:
+            assert sc[0, 0] == g["pow2_scale_group0"]
+        else:
+            assert sc[0, 0] == g["ue8m0_byte_group0"] and sc[0, 1] == g["ue8m0_byte_group1_zeros"]
+    for i, b in g["tensor_extra_value"].items():
+        x[0, int(i)] = int(b, 16)
+    q, sc = oracle.quantize_rows(x, 3, g["tensor_scale"])
+    exp = np.zeros(H, np.uint8)
+    for i, c in g["tensor_codes"].items():
+        exp[int(i)] = int(c, 16)
+    np.testing.assert_array_equal(q[0], exp)
+    assert np.all(sc == np.float32(g["tensor_scale"]))
