@@ -22,6 +22,8 @@ __all__ = [
     "EP_DEVERR_BAD_EXPERT", "EP_DEVERR_RECV_OVERFLOW", "EP_DEVERR_SLOT_OVERFLOW",
     "EP_BF16", "EP_FP8_E4M3", "EP_COMBINE_SUM", "EP_COMBINE_WEIGHTED",
     "EP_PHASE_SEND", "EP_PHASE_RECV", "EP_PHASE_BOTH", "EP_MAX_RANKS",
+    "EP_FP8_SCALE_FP32", "EP_FP8_SCALE_POW2", "EP_FP8_SCALE_UE8M0", "EP_FP8_SCALE_TENSOR",
+    "ep_fp8_options",
     "EpError", "ep_shape", "ep_launch", "ep_layout", "ep_handle", "ep_recv", "ep_ll_buffer",
     "lib", "library_path", "make_shape", "make_launch",
     "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
@@ -35,6 +37,7 @@ EP_DEVERR_BAD_EXPERT, EP_DEVERR_RECV_OVERFLOW, EP_DEVERR_SLOT_OVERFLOW = 1, 2, 4
 EP_BF16, EP_FP8_E4M3 = 0, 1
 EP_COMBINE_SUM, EP_COMBINE_WEIGHTED = 0, 1
 EP_PHASE_SEND, EP_PHASE_RECV, EP_PHASE_BOTH = 1, 2, 3
+EP_FP8_SCALE_FP32, EP_FP8_SCALE_POW2, EP_FP8_SCALE_UE8M0, EP_FP8_SCALE_TENSOR = 0, 1, 2, 3
 EP_MAX_RANKS = 64
 
 # Every function include/ep.h declares (checked by the ABI test).
@@ -67,6 +70,10 @@ class ep_shape(ctypes.Structure):
                 ("num_max_dispatch_tokens_per_rank", _I32), ("num_sms", _I32)]
 
 
+class ep_fp8_options(ctypes.Structure):
+    _fields_ = [("scale_format", _I32), ("tensor_scale", ctypes.c_float)]
+
+
 class ep_launch(ctypes.Structure):
     _fields_ = [("stream", _P), ("wait_event", _P), ("record_event", _P), ("error_flags", _P)]
 
@@ -85,12 +92,14 @@ class ep_handle(ctypes.Structure):
 
 class ep_recv(ctypes.Structure):
     _fields_ = [("recv_x", _P), ("recv_x_scales", _P), ("recv_topk_idx", _P),
-                ("recv_topk_weights", _P), ("recv_src_idx", _P), ("row_offset", _P)]
+                ("recv_topk_weights", _P), ("recv_src_idx", _P), ("row_offset", _P),
+                ("fp8", ep_fp8_options)]
 
 
 class ep_ll_buffer(ctypes.Structure):
     _fields_ = [("recv_x", _P), ("recv_x_scales", _P), ("src_info", _P), ("slot", _P),
-                ("send_count", _P), ("recv_expert_count", _P), ("layout_range", _P)]
+                ("send_count", _P), ("recv_expert_count", _P), ("layout_range", _P),
+                ("fp8", ep_fp8_options)]
 
 
 _lib = None
@@ -228,11 +237,12 @@ def _offsets(row_offset: Sequence[int]):
 def ep_dispatch(shape: ep_shape, x, x_dtype: int, x_scales, recv_dtype: int, topk_idx,
                 topk_weights, handle: ep_handle, recv_x, recv_x_scales, recv_topk_idx,
                 recv_topk_weights, recv_src_idx, row_offset: Sequence[int],
-                launch: Optional[ep_launch] = None) -> None:
+                launch: Optional[ep_launch] = None, fp8_scale: int = EP_FP8_SCALE_FP32,
+                tensor_scale: float = 0.0) -> None:
     off = _offsets(row_offset)
     out = ep_recv(_ptr(recv_x), _ptr(recv_x_scales), _ptr(recv_topk_idx),
                   _ptr(recv_topk_weights), _ptr(recv_src_idx),
-                  ctypes.cast(off, ctypes.c_void_p))
+                  ctypes.cast(off, ctypes.c_void_p), ep_fp8_options(fp8_scale, tensor_scale))
     st = lib().ep_dispatch(ctypes.byref(shape), _ptr(x), x_dtype, _ptr(x_scales), recv_dtype,
                            _ptr(topk_idx), _ptr(topk_weights), ctypes.byref(handle),
                            ctypes.byref(out), ctypes.byref(_launch(launch)))

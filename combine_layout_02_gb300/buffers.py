@@ -9,8 +9,8 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (EP_BF16, EP_FP8_E4M3, ep_handle, ep_layout, ep_layout_workspace_size,
-               ep_ll_buffer, ep_shape, _ptr)
+from . import (EP_BF16, EP_FP8_E4M3, EP_FP8_SCALE_FP32, EP_FP8_SCALE_UE8M0, ep_fp8_options,
+               ep_handle, ep_layout, ep_layout_workspace_size, ep_ll_buffer, ep_shape, _ptr)
 
 
 def new_event(stream=None) -> torch.cuda.Event:
@@ -63,21 +63,22 @@ class RecvBuffers:
     """Receive buffers of a normal dispatch over `rows` rows (all destinations)."""
 
     def __init__(self, rows: int, H: int, k: int, recv_dtype: int = EP_BF16, with_topk=True,
-                 device="cuda", fill: Optional[int] = None):
+                 device="cuda", fill: Optional[int] = None, fp8_scale: int = EP_FP8_SCALE_FP32):
         self.rows = rows
         if recv_dtype == EP_BF16:
             self.recv_x = torch.empty((rows, H), dtype=torch.bfloat16, device=device)
             self.recv_x_scales = None
         else:
             self.recv_x = torch.empty((rows, H), dtype=torch.uint8, device=device)
-            self.recv_x_scales = torch.empty((rows, H // 128), dtype=torch.float32, device=device)
+            sdt = torch.uint8 if fp8_scale == EP_FP8_SCALE_UE8M0 else torch.float32
+            self.recv_x_scales = torch.empty((rows, H // 128), dtype=sdt, device=device)
         self.recv_topk_idx = torch.empty((rows, k), dtype=torch.int64, device=device) if with_topk else None
         self.recv_topk_weights = torch.empty((rows, k), dtype=torch.float32, device=device) if with_topk else None
         self.recv_src_idx = torch.empty((rows,), dtype=torch.int32, device=device)
         if fill is not None:
             self.recv_x.view(torch.uint8).fill_(fill)
             if self.recv_x_scales is not None:
-                self.recv_x_scales.fill_(float("nan"))
+                self.recv_x_scales.fill_(0xEE if self.recv_x_scales.dtype == torch.uint8 else float("nan"))
             if with_topk:
                 self.recv_topk_idx.fill_(-99)
                 self.recv_topk_weights.fill_(-5.0)
@@ -87,16 +88,19 @@ class RecvBuffers:
 class LLBuffers:
     """Low-latency receive buffers and handle for one shape."""
 
-    def __init__(self, shape: ep_shape, use_fp8: bool, device="cuda", fill: Optional[int] = None):
+    def __init__(self, shape: ep_shape, use_fp8: bool, device="cuda", fill: Optional[int] = None,
+                 fp8_scale: int = EP_FP8_SCALE_FP32, tensor_scale: float = 0.0):
         R, T, H, E, k = (shape.num_ranks, shape.num_tokens, shape.hidden, shape.num_experts,
                          shape.num_topk)
         nmax = shape.num_max_dispatch_tokens_per_rank
         E_loc = E // R
         slots = R * nmax
         i32 = dict(dtype=torch.int32, device=device)
+        self.fp8 = ep_fp8_options(fp8_scale, tensor_scale)
         if use_fp8:
             self.recv_x = torch.empty((R, E_loc, slots, H), dtype=torch.uint8, device=device)
-            self.recv_x_scales = torch.empty((R, E_loc, slots, H // 128), dtype=torch.float32, device=device)
+            sdt = torch.uint8 if fp8_scale == EP_FP8_SCALE_UE8M0 else torch.float32
+            self.recv_x_scales = torch.empty((R, E_loc, slots, H // 128), dtype=sdt, device=device)
         else:
             self.recv_x = torch.empty((R, E_loc, slots, H), dtype=torch.bfloat16, device=device)
             self.recv_x_scales = None
@@ -112,7 +116,7 @@ class LLBuffers:
     def struct(self) -> ep_ll_buffer:
         return ep_ll_buffer(_ptr(self.recv_x), _ptr(self.recv_x_scales), _ptr(self.src_info),
                             _ptr(self.slot), _ptr(self.send_count), _ptr(self.recv_expert_count),
-                            _ptr(self.layout_range))
+                            _ptr(self.layout_range), self.fp8)
 
 
 def compact_row_offsets(counts: Sequence[int]) -> list:

@@ -31,7 +31,7 @@ struct DispatchArgs {
     const float* topk_weights;      // nullable
     const int32_t* send_head;
     char* recv_x;
-    float* recv_x_scales;
+    void* recv_x_scales;
     int64_t* recv_topk_idx;
     float* recv_topk_weights;
     int32_t* recv_src_idx;
@@ -39,6 +39,7 @@ struct DispatchArgs {
     int R, T, H, k, E_loc;
     int in_elem;                    // bytes per element of x
     int copy_scales;                // pre-quantised input: copy x_scales rows too
+    QuantMode qm;                   // fused quantisation: scale format
     int64_t ntok;                   // R * T
     uint32_t* err;
 };
@@ -103,12 +104,13 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
             scatter_copy_row<U>(src, a.recv_x, s_row[warp], nd, out_row_bytes, lane, 32);
             if (a.copy_scales) {
                 const float* ss = a.x_scales + g * G;
+                float* rs = reinterpret_cast<float*>(a.recv_x_scales);
                 for (int p = 0; p < nd; ++p)
-                    for (int i = lane; i < G; i += 32) a.recv_x_scales[s_row[warp][p] * G + i] = ss[i];
+                    for (int i = lane; i < G; i += 32) rs[s_row[warp][p] * G + i] = ss[i];
             }
         } else {
             scatter_quant_row<U>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
-                                 s_row[warp], nd, a.H, lane, 32);
+                                 s_row[warp], nd, a.H, a.qm, lane, 32);
         }
         __syncwarp();
     }
@@ -159,6 +161,14 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     if (topk_weights == nullptr && out->recv_topk_weights != nullptr) return EP_ERR_INVALID_ARG;
     // 16-byte vector access of rows.
     if (((uintptr_t)x & 15) != 0 || ((uintptr_t)out->recv_x & 15) != 0) return EP_ERR_INVALID_ARG;
+    // Scale formats other than per-group fp32 apply to a fused quantisation only.
+    const int fmt = out->fp8.scale_format;
+    if (fmt < EP_FP8_SCALE_FP32 || fmt > EP_FP8_SCALE_TENSOR) return EP_ERR_INVALID_ARG;
+    const bool fused = x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3;
+    if (fmt != EP_FP8_SCALE_FP32 && !fused) return EP_ERR_INVALID_ARG;
+    if (fmt == EP_FP8_SCALE_TENSOR &&
+        !(out->fp8.tensor_scale > 0.0f && out->fp8.tensor_scale <= 3.4028234e38f))
+        return EP_ERR_INVALID_ARG;
 
     DispatchArgs a{};
     if ((st = load_row_offsets(out->row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
@@ -179,6 +189,9 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     a.E_loc = sh->num_experts / sh->num_ranks;
     a.in_elem = x_dtype == EP_BF16 ? 2 : 1;
     a.copy_scales = x_dtype == EP_FP8_E4M3 ? 1 : 0;
+    a.qm.mode = fmt;
+    a.qm.tscale = out->fp8.tensor_scale;
+    a.qm.tinv = fmt == EP_FP8_SCALE_TENSOR ? 1.0f / out->fp8.tensor_scale : 0.0f;
     a.ntok = ntok;
     a.err = launch->error_flags;
 

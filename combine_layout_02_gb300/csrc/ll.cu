@@ -34,7 +34,7 @@ struct LLArgs {
     const int64_t* topk_idx;
     const float* topk_weights;
     char* recv_x;
-    float* recv_x_scales;
+    void* recv_x_scales;
     int32_t* src_info;
     int32_t* slot;
     int32_t* send_count;
@@ -44,6 +44,7 @@ struct LLArgs {
     char* out;
     int R, T, H, E, k, E_loc, nmax, use_fp8, write_recv;
     int col_split;                  // combine: blocks per token (column ranges)
+    QuantMode qm;                   // send phase with use_fp8: scale format
     uint32_t* err;
 };
 
@@ -167,11 +168,13 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
         for (int i = 0; i < 2; ++i) {            // the prefetched units (all lanes shuffle)
             const int u = threadIdx.x + i * kThreads;
             float scale;
-            const uint4 q = quant_unit(pre[2 * i], pre[2 * i + 1], scale);
-            if (u < qunits) store_quant_unit(q_base, a.recv_x_scales, s_rows, nv, a.H, u, q, scale);
+            uint32_t sbyte;
+            const uint4 q = quant_unit(pre[2 * i], pre[2 * i + 1], a.qm, scale, sbyte);
+            if (u < qunits)
+                store_quant_unit(q_base, a.recv_x_scales, s_rows, nv, a.H, u, q, scale, sbyte, a.qm.mode);
         }
-        scatter_quant_row<1>(src, q_base, a.recv_x_scales, s_rows, nv, a.H, threadIdx.x, kThreads,
-                             2 * kThreads);
+        scatter_quant_row<1>(src, q_base, a.recv_x_scales, s_rows, nv, a.H, a.qm, threadIdx.x,
+                             kThreads, 2 * kThreads);
     } else {
         for (int p = 0; p < nv; ++p) {
             char* dst = a.recv_x + s_rows[p] * (int64_t)a.H * 2;
@@ -276,6 +279,12 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
             return EP_ERR_INVALID_ARG;
         if (sh->num_tokens > 0 && (x == nullptr || topk_idx == nullptr)) return EP_ERR_INVALID_ARG;
         if (use_fp8 && buf->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
+        const int fmt = buf->fp8.scale_format;
+        if (fmt < EP_FP8_SCALE_FP32 || fmt > EP_FP8_SCALE_TENSOR) return EP_ERR_INVALID_ARG;
+        if (fmt != EP_FP8_SCALE_FP32 && !use_fp8) return EP_ERR_INVALID_ARG;
+        if (fmt == EP_FP8_SCALE_TENSOR &&
+            !(buf->fp8.tensor_scale > 0.0f && buf->fp8.tensor_scale <= 3.4028234e38f))
+            return EP_ERR_INVALID_ARG;
         if (((uintptr_t)x & 15) != 0 || ((uintptr_t)buf->recv_x & 15) != 0) return EP_ERR_INVALID_ARG;
     }
     if ((phase & EP_PHASE_RECV) && (buf->recv_expert_count == nullptr || buf->layout_range == nullptr))
@@ -300,6 +309,9 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     a.nmax = sh->num_max_dispatch_tokens_per_rank;
     a.use_fp8 = use_fp8 ? 1 : 0;
     a.write_recv = (phase & EP_PHASE_RECV) ? 1 : 0;
+    a.qm.mode = buf->fp8.scale_format;
+    a.qm.tscale = buf->fp8.tensor_scale;
+    a.qm.tinv = a.qm.mode == EP_FP8_SCALE_TENSOR ? 1.0f / buf->fp8.tensor_scale : 0.0f;
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;

@@ -43,16 +43,25 @@ __device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
 }
 
 // FP8 e4m3 quantisation, one scale per 128 channels ("DeepEP" README feature notes:
-// FP8 dispatch with per-group scales). Unit = 16 channels (32 bytes of bf16 in, 16
-// bytes of e4m3 out); 8 consecutive units (8 consecutive lanes) form one group, so the
-// group amax is a 3-step xor-shuffle. `stride` must be a multiple of 32 and `first`
-// the thread's index in a block or warp whose size is `stride`; every lane of a warp
-// must call this (the shuffles use the full mask).
-//   amax' = max(amax, 1e-4), scale = amax' / 448 (IEEE division),
-//   inv = 448 / amax' (IEEE division), q = e4m3_rn_satfinite(x * inv).
-// Quantises one unit (16 bf16 channels held in a, b) to 16 e4m3 bytes and returns the
-// group scale. Must be called by all 32 lanes of the warp together (8-lane shuffles).
-__device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, float& scale) {
+// FP8 dispatch with per-group scales; round_scale; use_ue8m0; fp8_quant_scale). Unit =
+// 16 channels (32 bytes of bf16 in, 16 bytes of e4m3 out); 8 consecutive units (8
+// consecutive lanes) form one group, so the group amax is a 3-step xor-shuffle. Every
+// lane of a warp must call quant_unit together (the shuffles use the full mask).
+//   amax' = max(amax, 1e-4); s0 = amax' / 448 (IEEE division);
+//   FP32:   scale = s0, inv = 448 / amax' (IEEE division)
+//   POW2 / UE8M0: scale = 2^ceil(log2(s0)) from the exponent bits, inv = 1 / scale (exact)
+//   TENSOR: scale and inv given by the caller (inv = 1/s, IEEE division on the host)
+//   q = e4m3_rn_satfinite(x * inv).
+struct QuantMode {
+    int mode;          // ep_fp8_scale
+    float tscale;      // EP_FP8_SCALE_TENSOR
+    float tinv;        // 1 / tscale
+};
+
+// Quantises one unit (16 bf16 channels held in a, b) to 16 e4m3 bytes. Returns the
+// group scale (fp32) and its biased exponent byte (power-of-two modes).
+__device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, const QuantMode& qm,
+                                            float& scale, uint32_t& scale_byte) {
     const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     float f[16];
 #pragma unroll
@@ -60,15 +69,32 @@ __device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, floa
         f[2 * j] = bf16_lo(w[j]);
         f[2 * j + 1] = bf16_hi(w[j]);
     }
-    float amax = 0.0f;
+    float inv;
+    scale_byte = 0;
+    if (qm.mode == EP_FP8_SCALE_TENSOR) {
+        scale = qm.tscale;
+        inv = qm.tinv;
+    } else {
+        float amax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-    const float am = fmaxf(amax, 1e-4f);
-    scale = __fdiv_rn(am, 448.0f);
-    const float inv = __fdiv_rn(448.0f, am);
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+        const float am = fmaxf(amax, 1e-4f);
+        if (qm.mode == EP_FP8_SCALE_FP32) {
+            scale = __fdiv_rn(am, 448.0f);
+            inv = __fdiv_rn(448.0f, am);
+        } else {
+            // s0 >= 1e-4/448 and <= bf16 max/448, so it is a normal number and the
+            // rounded-up power of two and its reciprocal are normal too.
+            const uint32_t bits = __float_as_uint(__fdiv_rn(am, 448.0f));
+            const uint32_t e = ((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) != 0u ? 1u : 0u);
+            scale = __uint_as_float(e << 23);
+            inv = __uint_as_float((254u - e) << 23);
+            scale_byte = e;
+        }
+    }
     uint32_t qw[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -79,24 +105,31 @@ __device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, floa
     return make_uint4(qw[0], qw[1], qw[2], qw[3]);
 }
 
-// Stores one quantised unit u (and, for the first unit of a group, its scale) to every
-// destination row.
-__device__ __forceinline__ void store_quant_unit(uint8_t* __restrict__ q_base, float* __restrict__ s_base,
+// Stores one quantised unit u (and, for the first unit of a group, its scale: fp32, or
+// one byte in the UE8M0 mode) to every destination row.
+__device__ __forceinline__ void store_quant_unit(uint8_t* __restrict__ q_base, void* __restrict__ s_base,
                                                  const int64_t* rows, int nd, int H, int u,
-                                                 const uint4& q, float scale) {
+                                                 const uint4& q, float scale, uint32_t scale_byte,
+                                                 int mode) {
     const int G = H >> 7;
     for (int p = 0; p < nd; ++p) {
         st_v4(q_base + rows[p] * (int64_t)H + (int64_t)u * 16, q);
-        if ((u & 7) == 0) s_base[rows[p] * (int64_t)G + (u >> 3)] = scale;
+        if ((u & 7) == 0) {
+            if (mode == EP_FP8_SCALE_UE8M0)
+                reinterpret_cast<uint8_t*>(s_base)[rows[p] * (int64_t)G + (u >> 3)] = (uint8_t)scale_byte;
+            else
+                reinterpret_cast<float*>(s_base)[rows[p] * (int64_t)G + (u >> 3)] = scale;
+        }
     }
 }
 
 template <int U>
 __device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
                                                   uint8_t* __restrict__ q_base,
-                                                  float* __restrict__ s_base,
+                                                  void* __restrict__ s_base,
                                                   const int64_t* rows, int nd, int H,
-                                                  int first, int stride, int u_start = 0) {
+                                                  const QuantMode& qm, int first, int stride,
+                                                  int u_start = 0) {
     const int units = H >> 4;
     for (int u0 = u_start; u0 < units; u0 += stride * U) {
         uint4 a[U], b[U];
@@ -115,8 +148,9 @@ __device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
         for (int i = 0; i < U; ++i) {
             const int u = u0 + i * stride + first;
             float scale;
-            const uint4 q = quant_unit(a[i], b[i], scale);
-            if (u < units) store_quant_unit(q_base, s_base, rows, nd, H, u, q, scale);
+            uint32_t sbyte;
+            const uint4 q = quant_unit(a[i], b[i], qm, scale, sbyte);
+            if (u < units) store_quant_unit(q_base, s_base, rows, nd, H, u, q, scale, sbyte, qm.mode);
         }
     }
 }

@@ -78,6 +78,28 @@ typedef enum ep_dtype { EP_BF16 = 0, EP_FP8_E4M3 = 1 } ep_dtype;
 typedef enum ep_combine_mode { EP_COMBINE_SUM = 0, EP_COMBINE_WEIGHTED = 1 } ep_combine_mode;
 typedef enum ep_phase { EP_PHASE_SEND = 1, EP_PHASE_RECV = 2, EP_PHASE_BOTH = 3 } ep_phase;
 
+/* Scale format of a fused FP8 quantisation ([README] feature notes: FP8 dispatch with
+ * per-group scales; round_scale; use_ue8m0, also for the low-latency kernels; a single
+ * per-tensor scale fp8_quant_scale). Groups are 128 channels; amax' = max(amax, 1e-4).
+ *   EP_FP8_SCALE_FP32   scale = amax'/448 (fp32), q = e4m3(x * (448/amax'))  [default]
+ *   EP_FP8_SCALE_POW2   scale = 2^ceil(log2(amax'/448)) (fp32), q = e4m3(x / scale)
+ *   EP_FP8_SCALE_UE8M0  as POW2, but each scale is stored as one byte, its biased
+ *                       exponent (scale = 2^(byte - 127)); recv_x_scales is uint8
+ *   EP_FP8_SCALE_TENSOR every group uses the caller's tensor_scale s (> 0, finite):
+ *                       q = e4m3(x * (1/s)); s is written to every scale slot
+ * q is rounded to nearest even and saturated to +-448 (OCP E4M3). */
+typedef enum ep_fp8_scale {
+    EP_FP8_SCALE_FP32 = 0,
+    EP_FP8_SCALE_POW2 = 1,
+    EP_FP8_SCALE_UE8M0 = 2,
+    EP_FP8_SCALE_TENSOR = 3
+} ep_fp8_scale;
+
+typedef struct ep_fp8_options {
+    int32_t scale_format;   /* ep_fp8_scale; 0 (zero-initialised) = EP_FP8_SCALE_FP32 */
+    float tensor_scale;     /* EP_FP8_SCALE_TENSOR only */
+} ep_fp8_options;
+
 /* Problem shape. num_sms caps the grid of the copy kernels (0 = every SM of the
  * device); it plays the role of Buffer.set_num_sms in [README]. */
 typedef struct ep_shape {
@@ -153,19 +175,23 @@ typedef struct ep_handle {
  * R+1 non-decreasing int64 (worst case: row_offset[d] = d*R*T needs no host sync;
  * exact sizes need ep_read_recv_counts_sync first -- the pages' implicit CPU wait).
  *   recv_x            dev [rows][H] bf16 or e4m3 (per recv_dtype)
- *   recv_x_scales     dev [rows][H/128] fp32 (e4m3 only; dequantise as q * scale)
+ *   recv_x_scales     dev [rows][H/128] fp32, or uint8 with EP_FP8_SCALE_UE8M0 (e4m3
+ *                     only; dequantise as q * scale)
  *   recv_topk_idx     dev [rows][k] int64: local expert id (e - d*E_loc) if the entry's
  *                     expert lives on d, else -1. Written only when topk_idx is given.
  *   recv_topk_weights dev [rows][k] fp32: the weight if local, else 0. Written only
  *                     when topk_idx and topk_weights are given.
- *   recv_src_idx      dev [rows] int32 (nullable): token index of each row. */
+ *   recv_src_idx      dev [rows] int32 (nullable): token index of each row.
+ *   fp8               scale format of a fused quantisation (bf16 x, e4m3 receive);
+ *                     must be EP_FP8_SCALE_FP32 for other dtype combinations. */
 typedef struct ep_recv {
     void* recv_x;
-    float* recv_x_scales;
+    void* recv_x_scales;
     int64_t* recv_topk_idx;
     float* recv_topk_weights;
     int32_t* recv_src_idx;
     const int64_t* row_offset;
+    ep_fp8_options fp8;
 } ep_recv;
 
 /* Low-latency buffers and handle ([README] low-latency example; [HOOK]). All dev.
@@ -173,22 +199,25 @@ typedef struct ep_recv {
  * expert el, R*Nmax fixed slots; source s owns slots [s*Nmax, (s+1)*Nmax), filled in
  * token order.
  *   recv_x            [R][E_loc][R*Nmax][H] e4m3 (use_fp8) or bf16
- *   recv_x_scales     [R][E_loc][R*Nmax][H/128] fp32 (use_fp8 only)
+ *   recv_x_scales     [R][E_loc][R*Nmax][H/128] fp32, or uint8 with
+ *                     EP_FP8_SCALE_UE8M0 (use_fp8 only)
  *   src_info          [R][E_loc][R*Nmax] int32: token index of each filled slot
  *   slot              [R][T][k] int32: slot of entry (s, t, j), -1 if masked/skipped
  *   send_count        [R][E_loc][R] int32: per (d, el, s) count signal, written by
  *                     the send phase and read by the receive phase
  *   recv_expert_count [R][E_loc] int32 (int32 as in the port)
  *   layout_range      [R][E_loc][R][2] int32: (first slot, count) per source
+ *   fp8               scale format when use_fp8 (see ep_fp8_scale)
  * Slots beyond each count are left unwritten (stale data of earlier calls). */
 typedef struct ep_ll_buffer {
     void* recv_x;
-    float* recv_x_scales;
+    void* recv_x_scales;
     int32_t* src_info;
     int32_t* slot;
     int32_t* send_count;
     int32_t* recv_expert_count;
     int32_t* layout_range;
+    ep_fp8_options fp8;
 } ep_ll_buffer;
 
 /* ---------------------------------------------------------------- layout */

@@ -64,12 +64,15 @@ class GpuRun:
         return {k: v.cpu().numpy() for k, v in self.lb.as_dict().items()}
 
     def dispatch(self, off, recv_dtype=ep.EP_BF16, with_topk=True, x=None, x_dtype=ep.EP_BF16,
-                 x_scales=None, fill=0xA5) -> RecvBuffers:
-        rb = RecvBuffers(off[-1], self.H, self.k, recv_dtype=recv_dtype, with_topk=with_topk, fill=fill)
+                 x_scales=None, fill=0xA5, fp8_scale=ep.EP_FP8_SCALE_FP32,
+                 tensor_scale=0.0) -> RecvBuffers:
+        rb = RecvBuffers(off[-1], self.H, self.k, recv_dtype=recv_dtype, with_topk=with_topk, fill=fill,
+                         fp8_scale=fp8_scale)
         ep.ep_dispatch(self.sh, self.x if x is None else x, x_dtype, x_scales, recv_dtype,
                        self.topk if with_topk else None, self.wts if with_topk else None,
                        self.lb.handle(rb.recv_src_idx), rb.recv_x, rb.recv_x_scales,
-                       rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx, off, self.launch)
+                       rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx, off, self.launch,
+                       fp8_scale=fp8_scale, tensor_scale=tensor_scale)
         return rb
 
     def combine(self, y: torch.Tensor, off, mode, recv_topk_weights=None) -> tuple:
@@ -80,8 +83,9 @@ class GpuRun:
                       recv_topk_weights, out, cw, self.launch)
         return out, cw
 
-    def ll_dispatch(self, use_fp8: bool, phase=ep.EP_PHASE_BOTH, buf: LLBuffers = None) -> LLBuffers:
-        buf = buf or LLBuffers(self.sh, use_fp8, fill=0x5A)
+    def ll_dispatch(self, use_fp8: bool, phase=ep.EP_PHASE_BOTH, buf: LLBuffers = None,
+                    fp8_scale=ep.EP_FP8_SCALE_FP32, tensor_scale=0.0) -> LLBuffers:
+        buf = buf or LLBuffers(self.sh, use_fp8, fill=0x5A, fp8_scale=fp8_scale, tensor_scale=tensor_scale)
         ep.ep_ll_dispatch(self.sh, self.x, self.topk, use_fp8, phase, buf.struct(), self.launch)
         return buf
 

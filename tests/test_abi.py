@@ -95,6 +95,22 @@ def test_invalid_arguments_rejected_on_host(ep):
     st = L.ep_ll_dispatch(ctypes.byref(sh_ll2), 0x7000, 0x8000, 0, 4, ctypes.byref(buf),
                           ctypes.byref(launch))
     assert st == ep.EP_ERR_INVALID_ARG
+    # FP8 scale options: unknown format, non-positive per-tensor scale, or a scale format
+    # without a fused quantisation
+    off3 = (ctypes.c_int64 * 3)(0, 8, 16)
+    for fmt, ts, rdt in ((7, 0.0, ep.EP_FP8_E4M3), (ep.EP_FP8_SCALE_TENSOR, 0.0, ep.EP_FP8_E4M3),
+                         (ep.EP_FP8_SCALE_TENSOR, float("nan"), ep.EP_FP8_E4M3),
+                         (ep.EP_FP8_SCALE_POW2, 0.0, ep.EP_BF16)):
+        o = ep.ep_recv(0x2000, 0x2800, None, None, None, ctypes.cast(off3, ctypes.c_void_p),
+                       ep.ep_fp8_options(fmt, ts))
+        st = L.ep_dispatch(ctypes.byref(sh), 0x3000, ep.EP_BF16, None, rdt, None, None,
+                           ctypes.byref(h), ctypes.byref(o), ctypes.byref(launch))
+        assert st == ep.EP_ERR_INVALID_ARG, (fmt, ts, rdt)
+    buf_b = ep.ep_ll_buffer(0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000,
+                            ep.ep_fp8_options(ep.EP_FP8_SCALE_UE8M0, 0.0))
+    st = L.ep_ll_dispatch(ctypes.byref(sh_ll2), 0x7000, 0x8000, 0, ep.EP_PHASE_SEND,
+                          ctypes.byref(buf_b), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG        # a scale format needs use_fp8
     # unsupported shape
     big = ep.make_shape(65, 4, 128, 65, 1)
     st = L.ep_dispatch(ctypes.byref(big), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,

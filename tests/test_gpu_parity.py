@@ -288,3 +288,67 @@ def test_ll_slot_overflow_flag():
     assert exp["bad_entries"] == 2 * 4
     np.testing.assert_array_equal(host_bits(buf.slot), exp["slot"])
     np.testing.assert_array_equal(host_bits(buf.recv_expert_count), exp["recv_expert_count"])
+
+
+# ----------------------------------------------------------------------------- FP8 scale modes
+
+MODES = [(ep.EP_FP8_SCALE_POW2, 0.0), (ep.EP_FP8_SCALE_UE8M0, 0.0), (ep.EP_FP8_SCALE_TENSOR, 0.0173)]
+
+
+def _cmp_scales(got, exp, mode):
+    if mode == ep.EP_FP8_SCALE_UE8M0:
+        np.testing.assert_array_equal(got, exp)
+    else:
+        np.testing.assert_array_equal(got.view(np.uint32), exp.view(np.uint32))
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "group8", "k32"])
+@pytest.mark.parametrize("mode,ts", MODES)
+def test_dispatch_fp8_scale_modes_bit_exact(name, mode, ts):
+    """round_scale / UE8M0 / per-tensor scale ("DeepEP" README feature notes)."""
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, fp8_scale=mode, tensor_scale=ts)
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, inp["topk_idx"],
+                          inp["topk_weights"], x_kind=oracle.X_QUANTIZE, scale_mode=mode,
+                          tensor_scale=ts)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    _cmp_scales(host_bits(rb.recv_x_scales), exp["recv_x_scales"], mode)
+    assert run.flags() == 0
+
+
+@pytest.mark.parametrize("mode,ts", MODES + [(ep.EP_FP8_SCALE_TENSOR, 1e-30)])
+def test_fp8_scale_modes_extreme_values(mode, ts):
+    R, T, H, E, k = 2, 8, 256, 4, 2
+    rng = np.random.default_rng(114)
+    x32 = rng.standard_normal((R, T, H)).astype(np.float32)
+    x32[0, 0] = 0.0
+    x32[0, 1, :128] = 3e-5
+    x32[0, 2] *= 1e30
+    x32[0, 3, 128:] = -1e-38
+    x32[1, 0, :] = np.tile(np.array([2.0, -3 / 1024, 1.0, 0.01], np.float32), H // 4)
+    xb = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    topk = np.tile(np.array([0, 3], np.int64), (R, T, 1))
+    inp = {"x": xb, "topk_idx": topk, "topk_weights": np.full((R, T, k), 0.5, np.float32)}
+    run = GpuRun(R, T, H, E, k, 1, inp)
+    ref = oracle.layout(topk, E, 1)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, with_topk=False, fp8_scale=mode, tensor_scale=ts)
+    exp = oracle.dispatch(xb, ref["send_head"], np.array(off), E, x_kind=oracle.X_QUANTIZE,
+                          scale_mode=mode, tensor_scale=ts)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    _cmp_scales(host_bits(rb.recv_x_scales), exp["recv_x_scales"], mode)
+
+
+@pytest.mark.parametrize("mode,ts", MODES)
+def test_ll_dispatch_scale_modes_bit_exact(mode, ts):
+    w, inp, run = _ll_setup("masked")
+    buf = run.ll_dispatch(True, fp8_scale=mode, tensor_scale=ts)
+    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, True, fill_x=0x5A,
+                             scale_mode=mode, tensor_scale=ts)
+    np.testing.assert_array_equal(host_bits(buf.recv_x), exp["recv_x"])
+    filled = exp["src_info"] != -7
+    _cmp_scales(host_bits(buf.recv_x_scales)[filled], exp["recv_x_scales"][filled], mode)
+    np.testing.assert_array_equal(host_bits(buf.slot), exp["slot"])
