@@ -44,6 +44,12 @@ def lib():
         L.oracle_ll_dispatch.restype = I64
         L.oracle_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P]
         L.oracle_ll_combine.restype = None
+        L.oracle_expert_layout.argtypes = [I, I, I, I, P, P, P]
+        L.oracle_expert_layout.restype = I64
+        L.oracle_dispatch_expert_major.argtypes = [I, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P, P]
+        L.oracle_dispatch_expert_major.restype = I64
+        L.oracle_combine_expert_major.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P]
+        L.oracle_combine_expert_major.restype = None
         _lib = L
     return _lib
 
@@ -239,4 +245,56 @@ def ll_combine(y: np.ndarray, topk_idx: np.ndarray, topk_weights: np.ndarray,
     out = np.empty((R, T, H), np.uint16)
     lib().oracle_ll_combine(R, T, H, E, k, nmax, _p(y), _p(topk_idx),
                             _p(_c(topk_weights, np.float32)), _p(_c(slot, np.int32)), _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- expert-major layout
+
+def expert_layout(topk_idx: np.ndarray, E: int) -> dict:
+    """Expert-major placement: expert_rows [R, T, k] (row in the destination's region or
+    -1) and expert_prefix [R, E_loc + 1] (exclusive per-expert prefix; last = total)."""
+    topk_idx = _c(topk_idx, np.int64)
+    R, T, k = topk_idx.shape
+    rows = np.empty((R, T, k), np.int32)
+    pre = np.empty((R, E // R + 1), np.int32)
+    bad = lib().oracle_expert_layout(R, T, E, k, _p(topk_idx), _p(rows), _p(pre))
+    return {"expert_rows": rows, "expert_prefix": pre, "bad_entries": int(bad)}
+
+
+def dispatch_expert_major(x, topk_idx, topk_weights, expert_rows, row_offset, E,
+                          quantize=False, scale_mode=SCALE_FP32, tensor_scale=0.0,
+                          fill_x=0, fill_src=-3, fill_w=-5.0) -> dict:
+    x = _c(x, np.uint16)
+    topk_idx = _c(topk_idx, np.int64)
+    R, T, H = x.shape
+    k = topk_idx.shape[-1]
+    row_offset = _c(row_offset, np.int64)
+    rows = int(row_offset[-1])
+    res = {"recv_x": np.full((rows, H), fill_x, np.uint8 if quantize else np.uint16),
+           "recv_src_idx": np.full((rows,), fill_src, np.int32),
+           "recv_weights": np.full((rows,), fill_w, np.float32)}
+    if quantize:
+        res["recv_x_scales"] = (np.full((rows, H // 128), 0xEE, np.uint8) if scale_mode == SCALE_UE8M0
+                                else np.full((rows, H // 128), np.nan, np.float32))
+    else:
+        res["recv_x_scales"] = None
+    bad = lib().oracle_dispatch_expert_major(
+        R, T, H, E, k, int(bool(quantize)), scale_mode, tensor_scale, _p(x), _p(topk_idx),
+        _p(_c(topk_weights, np.float32)), _p(_c(expert_rows, np.int32)), _p(row_offset),
+        _p(res["recv_x"]), _p(res["recv_x_scales"]), _p(res["recv_src_idx"]), _p(res["recv_weights"]))
+    res["bad_rows"] = int(bad)
+    return res
+
+
+def combine_expert_major(y, topk_idx, topk_weights, expert_rows, row_offset, E,
+                         weighted=True) -> np.ndarray:
+    topk_idx = _c(topk_idx, np.int64)
+    R, T, k = topk_idx.shape
+    y = _c(y, np.uint16)
+    H = y.shape[-1]
+    out = np.empty((R, T, H), np.uint16)
+    lib().oracle_combine_expert_major(R, T, H, E, k, int(bool(weighted)), _p(y),
+                                      _p(_c(row_offset, np.int64)), _p(topk_idx),
+                                      _p(_c(topk_weights, np.float32)), _p(_c(expert_rows, np.int32)),
+                                      _p(out))
     return out

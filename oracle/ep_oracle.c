@@ -569,3 +569,150 @@ EXPORT void oracle_ll_combine(int R, int T, int H, int E, int k, int nmax,
         }
     free(acc);
 }
+
+/* ------------------------------------------------------------------------- */
+/* Expert-major packed receive layout                                        */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * [README] low-latency example: the receive buffers come in a "specific format" for a
+ * grouped GEMM; for the normal kernels the same packing is the expert-major layout.
+ * Reading: destination d's region holds one row per valid entry (s, t, j) whose expert e
+ * lives on d, grouped by local expert el = e - d*E_loc (ascending), then by source rank,
+ * then by entry order (t, j):
+ *   expert_prefix[d][el]  = sum over el' < el of num_recv_tokens_per_expert[d][el']
+ *                           (expert_prefix[d][E_loc] = the region's row count)
+ *   expert_rows[s][t][j]  = expert_prefix[d][el] + sum over s' < s of
+ *                           num_tokens_per_expert[s'][e] + #{(t', j') < (t, j) of s with
+ *                           expert e}, or -1 for masked / invalid entries.
+ * Returns the number of entries outside [-1, E).
+ */
+EXPORT int64_t oracle_expert_layout(int R, int T, int E, int k, const int64_t* topk_idx,
+                                    int32_t* expert_rows, int32_t* expert_prefix)
+{
+    const int E_loc = E / R;
+    int64_t bad = 0;
+    int32_t* cnt = (int32_t*)calloc((size_t)R * E + 1, sizeof(int32_t));    /* [s][e] */
+    int32_t* run = (int32_t*)calloc((size_t)E + 1, sizeof(int32_t));
+    int32_t* base = (int32_t*)calloc((size_t)E + 1, sizeof(int32_t));
+
+    for (int s = 0; s < R; s++)
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                int64_t e = topk_idx[((int64_t)s * T + t) * k + j];
+                if (e == -1) continue;
+                if (e < 0 || e >= E) { bad++; continue; }
+                cnt[s * E + e] += 1;
+            }
+    for (int d = 0; d < R; d++) {
+        int32_t acc = 0;
+        for (int el = 0; el < E_loc; el++) {
+            expert_prefix[d * (E_loc + 1) + el] = acc;
+            for (int s = 0; s < R; s++) acc += cnt[s * E + d * E_loc + el];
+        }
+        expert_prefix[d * (E_loc + 1) + E_loc] = acc;
+    }
+    for (int s = 0; s < R; s++) {
+        for (int e = 0; e < E; e++) {
+            int d = e / E_loc, el = e % E_loc;
+            int32_t b = expert_prefix[d * (E_loc + 1) + el];
+            for (int sp = 0; sp < s; sp++) b += cnt[sp * E + e];
+            base[e] = b;
+            run[e] = 0;
+        }
+        for (int t = 0; t < T; t++)
+            for (int j = 0; j < k; j++) {
+                int64_t i = ((int64_t)s * T + t) * k + j;
+                int64_t e = topk_idx[i];
+                if (e < 0 || e >= E) { expert_rows[i] = -1; continue; }
+                expert_rows[i] = base[e] + run[e]++;
+            }
+    }
+    free(cnt);
+    free(run);
+    free(base);
+    return bad;
+}
+
+/*
+ * Expert-major dispatch: every valid entry (s, t, j) with expert e on rank d writes the
+ * token's row to recv_x[row_offset[d] + expert_rows[s][t][j]] (bf16 copy, or e4m3 with
+ * per-128-channel scales quantised once per token as in oracle_quantize_row_mode), and
+ * recv_src_idx[row] = t, recv_weights[row] = topk_weights[s][t][j] (one weight per row).
+ * Returns the number of rows outside their region.
+ */
+EXPORT int64_t oracle_dispatch_expert_major(int R, int T, int H, int E, int k, int quantize,
+                                            int scale_mode, float tensor_scale,
+                                            const uint16_t* x, const int64_t* topk_idx,
+                                            const float* topk_weights, const int32_t* expert_rows,
+                                            const int64_t* row_offset, void* recv_x,
+                                            void* recv_x_scales, int32_t* recv_src_idx,
+                                            float* recv_weights)
+{
+    const int E_loc = E / R;
+    const int G = H / 128;
+    const size_t scale_elem = scale_mode == 2 ? 1 : 4;
+    int64_t bad = 0;
+    uint8_t* qrow = (uint8_t*)malloc((size_t)H + 1);
+    float* srow = (float*)malloc(sizeof(float) * (size_t)(G + 1));
+    uint8_t* brow = (uint8_t*)malloc((size_t)G + 1);
+    for (int s = 0; s < R; s++)
+        for (int t = 0; t < T; t++) {
+            const int64_t tok = (int64_t)s * T + t;
+            const uint16_t* xrow = x + tok * H;
+            if (quantize) oracle_quantize_row_mode(xrow, H, scale_mode, tensor_scale, qrow, srow, brow);
+            for (int j = 0; j < k; j++) {
+                int64_t e = topk_idx[tok * k + j];
+                int32_t r = expert_rows[tok * k + j];
+                if (e < 0 || e >= E || r < 0) continue;
+                int d = (int)(e / E_loc);
+                int64_t row = row_offset[d] + r;
+                if (row >= row_offset[d + 1]) { bad++; continue; }
+                if (quantize) {
+                    memcpy((uint8_t*)recv_x + (size_t)row * H, qrow, (size_t)H);
+                    memcpy((uint8_t*)recv_x_scales + (size_t)row * G * scale_elem,
+                           scale_mode == 2 ? (const void*)brow : (const void*)srow, scale_elem * (size_t)G);
+                } else {
+                    memcpy((uint16_t*)recv_x + (size_t)row * H, xrow, sizeof(uint16_t) * (size_t)H);
+                }
+                if (recv_src_idx) recv_src_idx[row] = t;
+                if (recv_weights) recv_weights[row] = topk_weights[tok * k + j];
+            }
+        }
+    free(qrow);
+    free(srow);
+    free(brow);
+    return bad;
+}
+
+/*
+ * Expert-major combine: out[s][t] = sum over valid j (ascending) of
+ * c_j * y[row_offset[d] + expert_rows[s][t][j]], c_j = topk_weights[s][t][j] (weighted)
+ * or 1 (sum); binary64 accumulation, one bf16 rounding. A token with no valid entry
+ * gives +0.
+ */
+EXPORT void oracle_combine_expert_major(int R, int T, int H, int E, int k, int weighted,
+                                        const uint16_t* y, const int64_t* row_offset,
+                                        const int64_t* topk_idx, const float* topk_weights,
+                                        const int32_t* expert_rows, uint16_t* out)
+{
+    const int E_loc = E / R;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)(H + 1));
+    for (int s = 0; s < R; s++)
+        for (int t = 0; t < T; t++) {
+            const int64_t tok = (int64_t)s * T + t;
+            for (int h = 0; h < H; h++) acc[h] = 0.0;
+            for (int j = 0; j < k; j++) {
+                int64_t e = topk_idx[tok * k + j];
+                int32_t r = expert_rows[tok * k + j];
+                if (e < 0 || e >= E || r < 0) continue;
+                int d = (int)(e / E_loc);
+                int64_t row = row_offset[d] + r;
+                if (row >= row_offset[d + 1]) continue;
+                double c = weighted ? (double)topk_weights[tok * k + j] : 1.0;
+                for (int h = 0; h < H; h++) acc[h] += c * (double)bf16_bits_to_float(y[(size_t)row * H + h]);
+            }
+            for (int h = 0; h < H; h++) out[(size_t)tok * H + h] = double_to_bf16_rne(acc[h]);
+        }
+    free(acc);
+}
