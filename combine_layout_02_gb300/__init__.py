@@ -27,7 +27,8 @@ __all__ = [
     "EpError", "ep_shape", "ep_launch", "ep_layout", "ep_handle", "ep_recv", "ep_ll_buffer",
     "lib", "library_path", "make_shape", "make_launch",
     "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
-    "ep_dispatch", "ep_combine", "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
+    "ep_dispatch", "ep_combine", "ep_dispatch_expert_major", "ep_combine_expert_major",
+    "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
     "ep_read_error_flags_sync", "ep_kernel_launch_count", "ep_abi_version",
     "EXPORTED_SYMBOLS",
 ]
@@ -43,7 +44,7 @@ EP_MAX_RANKS = 64
 # Every function include/ep.h declares (checked by the ABI test).
 EXPORTED_SYMBOLS = (
     "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
-    "ep_dispatch", "ep_combine",
+    "ep_dispatch", "ep_combine", "ep_dispatch_expert_major", "ep_combine_expert_major",
     "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
     "ep_read_error_flags_sync", "ep_status_string", "ep_last_cuda_error",
     "ep_kernel_launch_count", "ep_abi_version",
@@ -87,7 +88,7 @@ class ep_handle(ctypes.Structure):
     _fields_ = [("rank_prefix_matrix", _P), ("channel_prefix_matrix", _P),
                 ("recv_channel_prefix_matrix", _P), ("recv_src_idx", _P),
                 ("is_token_in_rank", _P), ("send_head", _P),
-                ("num_recv_tokens_per_expert", _P)]
+                ("num_recv_tokens_per_expert", _P), ("expert_rows", _P), ("expert_prefix", _P)]
 
 
 class ep_recv(ctypes.Structure):
@@ -126,6 +127,10 @@ def lib():
                                   S(ep_handle), S(ep_recv), S(ep_launch)]
         L.ep_combine.argtypes = [S(ep_shape), _P, _P, S(ep_handle), ctypes.c_int, _P, _P, _P,
                                  _P, _P, S(ep_launch)]
+        L.ep_dispatch_expert_major.argtypes = [S(ep_shape), _P, ctypes.c_int, _P, _P, S(ep_handle),
+                                                S(ep_recv), S(ep_launch)]
+        L.ep_combine_expert_major.argtypes = [S(ep_shape), _P, _P, S(ep_handle), ctypes.c_int, _P, _P,
+                                               _P, S(ep_launch)]
         L.ep_ll_dispatch.argtypes = [S(ep_shape), _P, _P, ctypes.c_int, ctypes.c_int,
                                      S(ep_ll_buffer), S(ep_launch)]
         L.ep_ll_combine.argtypes = [S(ep_shape), _P, _P, _P, S(ep_ll_buffer), ctypes.c_int, _P,
@@ -141,7 +146,8 @@ def lib():
         L.ep_kernel_launch_count.restype = ctypes.c_uint64
         L.ep_abi_version.argtypes = []
         L.ep_abi_version.restype = _I32
-        for name in ("ep_get_layout", "ep_get_layout_static_scratch", "ep_dispatch", "ep_combine", "ep_ll_dispatch",
+        for name in ("ep_get_layout", "ep_get_layout_static_scratch", "ep_dispatch", "ep_combine",
+                     "ep_dispatch_expert_major", "ep_combine_expert_major", "ep_ll_dispatch",
                      "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
                      "ep_read_error_flags_sync"):
             getattr(L, name).restype = _I32
@@ -258,6 +264,29 @@ def ep_combine(shape: ep_shape, y, row_offset: Sequence[int], handle: ep_handle,
                           _ptr(recv_topk_weights), _ptr(out), _ptr(combined_topk_weights),
                           ctypes.byref(_launch(launch)))
     _check("ep_combine", st)
+
+
+def ep_dispatch_expert_major(shape: ep_shape, x, recv_dtype: int, topk_idx, topk_weights,
+                             handle: ep_handle, recv_x, recv_x_scales, recv_weights, recv_src_idx,
+                             row_offset: Sequence[int], launch: Optional[ep_launch] = None,
+                             fp8_scale: int = EP_FP8_SCALE_FP32, tensor_scale: float = 0.0) -> None:
+    off = _offsets(row_offset)
+    out = ep_recv(_ptr(recv_x), _ptr(recv_x_scales), None, _ptr(recv_weights), _ptr(recv_src_idx),
+                  ctypes.cast(off, ctypes.c_void_p), ep_fp8_options(fp8_scale, tensor_scale))
+    st = lib().ep_dispatch_expert_major(ctypes.byref(shape), _ptr(x), recv_dtype, _ptr(topk_idx),
+                                        _ptr(topk_weights), ctypes.byref(handle), ctypes.byref(out),
+                                        ctypes.byref(_launch(launch)))
+    _check("ep_dispatch_expert_major", st)
+
+
+def ep_combine_expert_major(shape: ep_shape, y, row_offset: Sequence[int], handle: ep_handle,
+                            mode: int, topk_idx, topk_weights, out,
+                            launch: Optional[ep_launch] = None) -> None:
+    off = _offsets(row_offset)
+    st = lib().ep_combine_expert_major(ctypes.byref(shape), _ptr(y), ctypes.cast(off, ctypes.c_void_p),
+                                       ctypes.byref(handle), mode, _ptr(topk_idx), _ptr(topk_weights),
+                                       _ptr(out), ctypes.byref(_launch(launch)))
+    _check("ep_combine_expert_major", st)
 
 
 def ep_ll_dispatch(shape: ep_shape, x, topk_idx, use_fp8: bool, phase: int, buf: ep_ll_buffer,

@@ -24,7 +24,7 @@ def new_event(stream=None) -> torch.cuda.Event:
 class LayoutBuffers:
     """Outputs of ep_get_layout plus the handle tensors and the layout workspace."""
 
-    def __init__(self, shape: ep_shape, device="cuda"):
+    def __init__(self, shape: ep_shape, device="cuda", expert_major: bool = False):
         R, T, E, C = shape.num_ranks, shape.num_tokens, shape.num_experts, shape.num_channels
         i32 = dict(dtype=torch.int32, device=device)
         self.shape = shape
@@ -39,6 +39,9 @@ class LayoutBuffers:
         ws = ep_layout_workspace_size(shape)
         self.workspace = torch.empty(max(ws, 16), dtype=torch.uint8, device=device)
         self.recv_src_idx: Optional[torch.Tensor] = None
+        k = shape.num_topk
+        self.expert_rows = torch.empty((R, T, k), **i32) if expert_major else None
+        self.expert_prefix = torch.empty((R, E // R + 1), **i32) if expert_major else None
 
     def layout(self) -> ep_layout:
         return ep_layout(_ptr(self.num_tokens_per_rank), None, _ptr(self.num_tokens_per_expert),
@@ -50,7 +53,8 @@ class LayoutBuffers:
         return ep_handle(_ptr(self.rank_prefix_matrix), _ptr(self.channel_prefix_matrix),
                          _ptr(self.recv_channel_prefix_matrix), _ptr(self.recv_src_idx),
                          _ptr(self.is_token_in_rank), _ptr(self.send_head),
-                         _ptr(self.num_recv_tokens_per_expert))
+                         _ptr(self.num_recv_tokens_per_expert), _ptr(self.expert_rows),
+                         _ptr(self.expert_prefix))
 
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k in (

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libep.so")
-SOURCES = ["ep_api.cu", "layout.cu", "layout_static.cu", "dispatch.cu", "combine.cu", "ll.cu"]
+SOURCES = ["ep_api.cu", "layout.cu", "layout_static.cu", "dispatch.cu", "combine.cu", "ll.cu",
+           "expert_major.cu"]
 HEADERS = ["ep_internal.cuh", "rowops.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",

@@ -42,6 +42,9 @@ struct LayoutArgs {
     int32_t* num_recv_per_expert;         // [R][E_loc] == [E]
     int32_t* ws_cnt;                      // [R][R][C]: (s*R + d)*C + c
     int32_t* ws_expert;                   // [R][C][E]: (s*C + c)*E + e
+    int32_t* expert_rows;                 // [R][T][k] nullable: expert-major placement
+    int32_t* expert_prefix;               // [R][E_loc + 1]
+    int ew;                               // bitmask words per expert (expert-major ranks)
     uint32_t* err;
 };
 
@@ -248,6 +251,109 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
     }
 }
 
+// ---- Expert-major placement (optional): rows of destination d grouped by local expert,
+// then source rank, then token. Runs after the two kernels above, which leave the
+// per-(source, channel) expert counts in the workspace.
+
+// One block per destination d. Per local expert (one warp each): exclusive scan of its
+// counts over (source, channel) in lexicographic order, in place in the workspace, and
+// the total; then the exclusive prefix of the totals over the local experts.
+__global__ void __launch_bounds__(kThreads) layout_expert_scan_kernel(LayoutArgs a) {
+    extern __shared__ int s_tot[];        // [E_loc]
+    const int d = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = a.R * a.C;
+    pdl_trigger();
+    pdl_wait();
+    for (int el = warp; el < a.E_loc; el += kWarps) {
+        const int e = d * a.E_loc + el;
+        int carry = 0;
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            const int v = i < n ? a.ws_expert[(int64_t)i * a.E + e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (i < n) a.ws_expert[(int64_t)i * a.E + e] = carry + incl - v;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) s_tot[el] = carry;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry = 0;
+        int32_t* pre = a.expert_prefix + (int64_t)d * (a.E_loc + 1);
+        for (int el0 = 0; el0 < a.E_loc; el0 += 32) {
+            const int el = el0 + lane;
+            const int v = el < a.E_loc ? s_tot[el] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (el < a.E_loc) pre[el] = carry + incl - v;
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (lane == 0) pre[a.E_loc] = carry;
+    }
+}
+
+// One block per (channel c, source s). Each entry's row = the expert's prefix on its
+// destination + the count of that expert in earlier (source, channel) pairs + the count
+// of earlier tokens of the channel with the same expert. The last term comes from
+// shared-memory bitmasks over sub-tiles of 32*ew tokens (one bit per token and expert,
+// set with atomicOr, then popc), so the result does not depend on thread timing.
+__global__ void __launch_bounds__(kThreads) layout_expert_rows_kernel(LayoutArgs a) {
+    extern __shared__ uint32_t esm[];
+    int* running = reinterpret_cast<int*>(esm);   // [E]
+    uint32_t* mask = esm + a.E;                    // [E][ew]
+    const int c = blockIdx.x, s = blockIdx.y, W = a.ew, sub = 32 * a.ew;
+    pdl_trigger();
+    pdl_wait();
+    for (int e = threadIdx.x; e < a.E; e += kThreads) {
+        const int d = e / a.E_loc, el = e - d * a.E_loc;
+        running[e] = a.expert_prefix[(int64_t)d * (a.E_loc + 1) + el] +
+                     a.ws_expert[((int64_t)s * a.C + c) * a.E + e];
+    }
+    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
+    const int lt = threadIdx.x;
+    for (int base = t0; base < t1; base += sub) {   // block-uniform trip count
+        for (int i = threadIdx.x; i < a.E * W; i += kThreads) mask[i] = 0u;
+        __syncthreads();
+        const int t = base + lt;
+        const bool mine = lt < sub && t < t1;
+        const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t) * a.k;
+        if (mine)
+            for (int j = 0; j < a.k; ++j) {
+                const int64_t e = row[j];
+                if (e >= 0 && e < a.E) atomicOr(&mask[e * W + (lt >> 5)], 1u << (lt & 31));
+            }
+        __syncthreads();
+        if (mine)
+            for (int j = 0; j < a.k; ++j) {
+                const int64_t e = row[j];
+                int r = -1;
+                if (e >= 0 && e < a.E) {
+                    const uint32_t* m = mask + e * W;
+                    r = running[e];
+                    for (int w = 0; w < (lt >> 5); ++w) r += __popc(m[w]);
+                    r += __popc(m[lt >> 5] & ((1u << (lt & 31)) - 1u));
+                }
+                a.expert_rows[((int64_t)s * a.T + t) * a.k + j] = r;
+            }
+        __syncthreads();
+        for (int e = threadIdx.x; e < a.E; e += kThreads) {
+            int add = 0;
+            for (int w = 0; w < W; ++w) add += __popc(mask[e * W + w]);
+            running[e] += add;
+        }
+        __syncthreads();
+    }
+}
+
 size_t ws_cnt_bytes(const ep_shape* sh) {
     const size_t n = (size_t)sh->num_ranks * sh->num_ranks * sh->num_channels * sizeof(int32_t);
     return (n + 255) & ~(size_t)255;
@@ -278,6 +384,11 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     if (sh->num_tokens > 0 && (handle->is_token_in_rank == nullptr || handle->send_head == nullptr))
         return EP_ERR_INVALID_ARG;
     if (layout != nullptr && layout->num_tokens_per_rdma_rank != nullptr) return EP_ERR_INVALID_ARG;
+    // Expert-major placement is optional: both outputs or neither.
+    const bool expert = handle->expert_rows != nullptr || handle->expert_prefix != nullptr;
+    if (expert && (handle->expert_prefix == nullptr || (sh->num_tokens > 0 && handle->expert_rows == nullptr)))
+        return EP_ERR_INVALID_ARG;
+    if (expert && sh->num_experts > EP_EXPERT_MAJOR_MAX_EXPERTS) return EP_ERR_UNSUPPORTED;
     if (sh->num_tokens > 0 && topk_idx == nullptr) return EP_ERR_INVALID_ARG;
     const size_t need = ep_layout_workspace_size(sh);
     if (workspace == nullptr || workspace_bytes < need || ((uintptr_t)workspace & 15) != 0)
@@ -312,6 +423,10 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     a.num_recv_per_expert = handle->num_recv_tokens_per_expert;
     a.ws_cnt = reinterpret_cast<int32_t*>(workspace);
     a.ws_expert = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + ws_cnt_bytes(sh));
+    a.expert_rows = handle->expert_rows;
+    a.expert_prefix = handle->expert_prefix;
+    // Bitmask words per expert: at most 6144 words (24 KB) of shared memory.
+    a.ew = expert ? (a.E >= 6144 ? 1 : (6144 / a.E > 16 ? 16 : 6144 / a.E)) : 1;
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;
@@ -320,6 +435,12 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     cudaError_t e = launch_pdl(layout_count_kernel, grid, dim3(kThreads), smem, launch->stream, a);
     if (e == cudaSuccess)
         e = launch_pdl(layout_prefix_kernel, grid, dim3(kThreads), 0, launch->stream, a);
+    if (e == cudaSuccess && expert)
+        e = launch_pdl(layout_expert_scan_kernel, dim3(a.R), dim3(kThreads), sizeof(int) * (size_t)a.E_loc,
+                       launch->stream, a);
+    if (e == cudaSuccess && expert)
+        e = launch_pdl(layout_expert_rows_kernel, grid, dim3(kThreads),
+                       sizeof(uint32_t) * (size_t)a.E * (1 + (size_t)a.ew), launch->stream, a);
     if (e != cudaSuccess) return cuda_fail(e);
     return end_call(launch);
 }

@@ -62,6 +62,7 @@ extern "C" {
 #define EP_MAX_TOPK 32
 #define EP_MAX_EXPERTS 8192
 #define EP_FP8_GROUP 128
+#define EP_EXPERT_MAJOR_MAX_EXPERTS 4096
 
 typedef int32_t ep_status;
 #define EP_OK 0
@@ -159,7 +160,16 @@ typedef struct ep_layout {
  *   send_head                  [R][T][R] int32: row of (s, t) in d's region, or -1;
  *                              rows of d are ordered by (source rank, token)
  *   num_recv_tokens_per_expert [R][E_loc] int32: rows rank d receives per local
- *                              expert (the pages' num_recv_tokens_per_expert_list) */
+ *                              expert (the pages' num_recv_tokens_per_expert_list)
+ * Optional expert-major placement (both NULL to skip; E <= EP_EXPERT_MAJOR_MAX_EXPERTS;
+ * reading of [README] low-latency example: received rows in a "specific format" for a
+ * grouped GEMM, here for the normal kernels): rank d's region holds one row per valid
+ * (token, k) entry whose expert lives on d, grouped by local expert, then source rank,
+ * then token. Experts within one token must be distinct for this placement.
+ *   expert_rows                [R][T][k] int32: row of entry (s, t, j) in its
+ *                              destination's region, -1 if masked
+ *   expert_prefix              [R][E_loc + 1] int32: first row of each local expert;
+ *                              [d][E_loc] = rows rank d receives (sum of its entries) */
 typedef struct ep_handle {
     int32_t* rank_prefix_matrix;
     int32_t* channel_prefix_matrix;
@@ -168,6 +178,8 @@ typedef struct ep_handle {
     uint8_t* is_token_in_rank;
     int32_t* send_head;
     int32_t* num_recv_tokens_per_expert;
+    int32_t* expert_rows;
+    int32_t* expert_prefix;
 } ep_handle;
 
 /* Receive buffers of a normal dispatch. Destination d's rows are
@@ -234,7 +246,8 @@ EP_API size_t ep_layout_workspace_size(const ep_shape* shape);
  *   handle    every field except recv_src_idx is written (recv_src_idx is ignored).
  *   workspace dev, >= ep_layout_workspace_size bytes, 16-byte aligned; contents need
  *             no initialisation and are overwritten.
- * Two kernels, no host synchronisation. Bad entries: EP_DEVERR_BAD_EXPERT. */
+ * Two kernels (four with the expert-major placement), no host synchronisation. Bad
+ * entries: EP_DEVERR_BAD_EXPERT. */
 EP_API ep_status ep_get_layout(const ep_shape* shape, const int64_t* topk_idx, ep_layout* layout,
                         ep_handle* handle, void* workspace, size_t workspace_bytes,
                         const ep_launch* launch);
@@ -310,6 +323,38 @@ EP_API ep_status ep_combine(const ep_shape* shape, const void* y, const int64_t*
                      const ep_handle* handle, ep_combine_mode mode, const int64_t* topk_idx,
                      const float* topk_weights, const float* recv_topk_weights, void* out,
                      float* combined_topk_weights, const ep_launch* launch);
+
+/* ---------------------------------------------------------------- expert-major layout */
+
+/* Dispatch into the expert-major packed layout (the handle's expert_rows from
+ * ep_get_layout; see ep_handle): one row per valid entry (s, t, j), written to
+ * recv_x[row_offset[d] + expert_rows[s][t][j]] where d owns the entry's expert. The row
+ * is bf16 (recv_dtype EP_BF16) or quantised once per token to e4m3 with out->fp8's
+ * scale format. Rows of local expert el on d start at expert_prefix[d][el]; size d's
+ * region with expert_prefix[d][E_loc] rows (after ep_read_recv_counts_sync-style read
+ * back) or with the worst case R*T*min(k, E_loc).
+ *   x             dev [R][T][H] bf16
+ *   topk_idx      dev [R][T][k] int64 (required), topk_weights dev [R][T][k] fp32 nullable
+ *   out           recv_x, recv_x_scales (e4m3), recv_src_idx [rows] (nullable: token
+ *                 index of each row), recv_topk_weights [rows] (nullable: the entry's
+ *                 weight, one per row), row_offset (host [R+1]); recv_topk_idx must be
+ *                 NULL (each row is one entry).
+ * Overflowing rows: EP_DEVERR_RECV_OVERFLOW. */
+EP_API ep_status ep_dispatch_expert_major(const ep_shape* shape, const void* x, ep_dtype recv_dtype,
+                                          const int64_t* topk_idx, const float* topk_weights,
+                                          const ep_handle* handle, ep_recv* out,
+                                          const ep_launch* launch);
+
+/* Combine from the expert-major layout: out[s][t] = sum over valid j (ascending) of
+ * c_j * y[y_row_offset[d] + expert_rows[s][t][j]], c_j = topk_weights[s][t][j]
+ * (EP_COMBINE_WEIGHTED) or 1 (EP_COMBINE_SUM); fp32 accumulation, one bf16 store.
+ *   y   dev [rows][H] bf16 (the grouped GEMM's output in the dispatch's row order)
+ *   out dev [R][T][H] bf16; a token with no valid entry gets +0 */
+EP_API ep_status ep_combine_expert_major(const ep_shape* shape, const void* y,
+                                         const int64_t* y_row_offset, const ep_handle* handle,
+                                         ep_combine_mode mode, const int64_t* topk_idx,
+                                         const float* topk_weights, void* out,
+                                         const ep_launch* launch);
 
 /* ---------------------------------------------------------------- low latency */
 
