@@ -217,6 +217,7 @@ def run_e2e(world, dev, stream, step, x, topk, wts, out, total_bytes, e2e_steps)
 
 
 PHASE_KERNEL = {"dispatch": "dispatch_kernel<copy>", "dispatch_fp8": "dispatch_kernel<quant>",
+                "dispatch_em": "dispatch_em_kernel<copy>", "combine_em": "combine_em_kernel",
                 "combine": "combine_kernel", "layout": "layout_count+layout_prefix",
                 "ll_send": "ll_send_kernel", "ll_recv": "ll_recv_kernel",
                 "ll_combine": "ll_combine_kernel"}
@@ -231,7 +232,16 @@ WORKLOAD_TEXT = {
                  "e4m3 dispatch send phase, receive phase, weighted bf16 combine; Nmax=128",
     "zipf_reuse": "R=16 x {T} tokens, hidden 4096, 128 experts, top-6 Zipf(1.2); layout once, "
                   "then dispatch(handle) of fresh x + weighted combine(handle)",
+    "dsv3_expert_major": "dsv3 shape; layout with the expert-major placement + expert-major bf16 "
+                         "dispatch (one row per token-expert entry, grouped per local expert) + "
+                         "weighted combine; worst-case regions R*T*min(k, E_loc) rows per rank",
 }
+
+
+def workload_config(name: str):
+    """The synthetic workload behind a bench workload name (the expert-major measurement
+    runs on the dsv3 workload)."""
+    return workloads.CONFIGS["dsv3" if name == "dsv3_expert_major" else name]
 
 
 def make_plan(args, ep, dev, stream, launch):
@@ -241,7 +251,7 @@ def make_plan(args, ep, dev, stream, launch):
     import torch
     from combine_layout_02_gb300.buffers import (LayoutBuffers, LLBuffers, RecvBuffers,
                                                  worst_case_row_offsets)
-    w = workloads.CONFIGS[args.workload]
+    w = workload_config(args.workload)
     if args.tokens:
         w = dataclasses.replace(w, T=args.tokens)
     if args.nmax:
@@ -318,6 +328,36 @@ def make_plan(args, ep, dev, stream, launch):
             return b, N
         plan["nbytes"] = nbytes
         plan["l2"] = "inputs larger than L2; no flush"
+    elif args.workload == "dsv3_expert_major":
+        sh = ep.make_shape(R, T, H, E, k, C)
+        lb = LayoutBuffers(sh, dev, expert_major=True)
+        cap = R * T * min(k, E // R)
+        off = [d * cap for d in range(R + 1)]
+        recv_x = torch.empty((off[-1], H), dtype=torch.bfloat16, device=dev)
+        recv_w = torch.empty((off[-1],), dtype=torch.float32, device=dev)
+        recv_src = torch.empty((off[-1],), dtype=torch.int32, device=dev)
+        out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+        layout_s, handle = lb.layout(), lb.handle()
+        plan["keep"] = (lb, recv_x, recv_w, recv_src, out)
+        plan["out"] = out
+        plan["phases"] = [
+            ("layout", lambda: ep.ep_get_layout(sh, topk, layout_s, handle, lb.workspace, launch)),
+            ("dispatch_em", lambda: ep.ep_dispatch_expert_major(sh, x, ep.EP_BF16, topk, wts, handle,
+                                                                recv_x, None, recv_w, recv_src, off,
+                                                                launch)),
+            ("combine_em", lambda: ep.ep_combine_expert_major(sh, recv_x, off, handle,
+                                                              ep.EP_COMBINE_WEIGHTED, topk, wts, out,
+                                                              launch)),
+        ]
+        plan["l2"] = "inputs larger than L2; no flush"
+
+        def nbytes():
+            M = int(lb.expert_prefix[:, -1].sum().item())
+            lay = Tt * k * 8 + Tt * R * (1 + 4) + Tt * k * (8 + 4)
+            return {"layout": lay,
+                    "dispatch_em": Tt * H * 2 + M * H * 2 + Tt * k * (8 + 4 + 4) + M * (4 + 4),
+                    "combine_em": M * H * 2 + Tt * H * 2 + Tt * k * (8 + 4 + 4)}, M
+        plan["nbytes"] = nbytes
     elif args.workload == "ll_decode":
         sh = ep.make_shape(R, T, H, E, k, C, nmax=w.nmax)
         buf = LLBuffers(sh, True, device=dev)
@@ -489,7 +529,7 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: " + WORKLOAD_TEXT[args.workload].format(T=w.T),
                    "R": w.R, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "C": w.C,
-                   "recv_rows" if args.workload != "ll_decode" else "valid_entries": units,
+                   "valid_entries" if args.workload in ("ll_decode", "dsv3_expert_major") else "recv_rows": units,
                    "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)",
                    "l2": plan["l2"]},
     }
@@ -500,7 +540,7 @@ def run_ours(args, rank, world):
             result[f"{short}_gbs"] = round(gbs[name], 1)
             result[f"{short}_frac_of_peak"] = round(gbs[name] / peak, 4)
     if "layout" in mean_ms:
-        dname = "dispatch_fp8" if "dispatch_fp8" in mean_ms else "dispatch"
+        dname = next(n for n in mean_ms if n.startswith("dispatch"))
         result["layout_dispatch_us"] = round((mean_ms["layout"] + mean_ms[dname]) * 1e3, 2)
     result["bytes_per_step"] = nbytes
     result["roofline"] = {"bound": "hbm", "kernel": PHASE_KERNEL[dom], "achieved": round(gbs[dom], 1),

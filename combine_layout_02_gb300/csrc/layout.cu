@@ -44,6 +44,7 @@ struct LayoutArgs {
     int32_t* ws_expert;                   // [R][C][E]: (s*C + c)*E + e
     int32_t* expert_rows;                 // [R][T][k] nullable: expert-major placement
     int32_t* expert_prefix;               // [R][E_loc + 1]
+    int32_t* ws_etot;                     // [E] expert totals (workspace)
     int ew;                               // bitmask words per expert (expert-major ranks)
     uint32_t* err;
 };
@@ -255,50 +256,38 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
 // then source rank, then token. Runs after the two kernels above, which leave the
 // per-(source, channel) expert counts in the workspace.
 
-// One block per destination d. Per local expert (one warp each): exclusive scan of its
-// counts over (source, channel) in lexicographic order, in place in the workspace, and
-// the total; then the exclusive prefix of the totals over the local experts.
+// One warp per expert e: exclusive scan of its counts over (source, channel) pairs in
+// lexicographic order, in place in the workspace, and its total (ws_etot[e]). Up to four
+// 32-value chunks are loaded before any is scanned, so most columns cost one round trip.
 __global__ void __launch_bounds__(kThreads) layout_expert_scan_kernel(LayoutArgs a) {
-    extern __shared__ int s_tot[];        // [E_loc]
-    const int d = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kWarps + warp;
     const int n = a.R * a.C;
     pdl_trigger();
     pdl_wait();
-    for (int el = warp; el < a.E_loc; el += kWarps) {
-        const int e = d * a.E_loc + el;
-        int carry = 0;
-        for (int i0 = 0; i0 < n; i0 += 32) {
-            const int i = i0 + lane;
-            const int v = i < n ? a.ws_expert[(int64_t)i * a.E + e] : 0;
-            int incl = v;
+    if (e >= a.E) return;
+    int carry = 0;
+    for (int i0 = 0; i0 < n; i0 += 128) {
+        int v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q * 32 + lane;
+            v[q] = i < n ? a.ws_expert[(int64_t)i * a.E + e] : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q * 32 + lane;
+            int incl = v[q];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
                 if (lane >= o) incl += y;
             }
-            if (i < n) a.ws_expert[(int64_t)i * a.E + e] = carry + incl - v;
+            if (i < n) a.ws_expert[(int64_t)i * a.E + e] = carry + incl - v[q];
             carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        if (lane == 0) s_tot[el] = carry;
     }
-    __syncthreads();
-    if (warp == 0) {
-        int carry = 0;
-        int32_t* pre = a.expert_prefix + (int64_t)d * (a.E_loc + 1);
-        for (int el0 = 0; el0 < a.E_loc; el0 += 32) {
-            const int el = el0 + lane;
-            const int v = el < a.E_loc ? s_tot[el] : 0;
-            int incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (el < a.E_loc) pre[el] = carry + incl - v;
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-        if (lane == 0) pre[a.E_loc] = carry;
-    }
+    if (lane == 0) a.ws_etot[e] = carry;
 }
 
 // One block per (channel c, source s). Each entry's row = the expert's prefix on its
@@ -309,45 +298,75 @@ __global__ void __launch_bounds__(kThreads) layout_expert_scan_kernel(LayoutArgs
 __global__ void __launch_bounds__(kThreads) layout_expert_rows_kernel(LayoutArgs a) {
     extern __shared__ uint32_t esm[];
     int* running = reinterpret_cast<int*>(esm);   // [E]
-    uint32_t* mask = esm + a.E;                    // [E][ew]
-    const int c = blockIdx.x, s = blockIdx.y, W = a.ew, sub = 32 * a.ew;
+    uint32_t* mask = esm + a.E;                    // [E][ew | 1]: odd stride, no bank conflicts
+    const int c = blockIdx.x, s = blockIdx.y, W = a.ew, WS = a.ew | 1, sub = 32 * a.ew;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     pdl_wait();
-    for (int e = threadIdx.x; e < a.E; e += kThreads) {
-        const int d = e / a.E_loc, el = e - d * a.E_loc;
-        running[e] = a.expert_prefix[(int64_t)d * (a.E_loc + 1) + el] +
-                     a.ws_expert[((int64_t)s * a.C + c) * a.E + e];
+    // Per destination d (one warp each): exclusive prefix of the expert totals over its
+    // local experts -> running[e]; block (0, 0) also writes expert_prefix.
+    for (int d = warp; d < a.R; d += kWarps) {
+        int carry = 0;
+        for (int el0 = 0; el0 < a.E_loc; el0 += 32) {
+            const int el = el0 + lane;
+            const int v = el < a.E_loc ? a.ws_etot[d * a.E_loc + el] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (el < a.E_loc) {
+                running[d * a.E_loc + el] = carry + incl - v;
+                if (c == 0 && s == 0) a.expert_prefix[(int64_t)d * (a.E_loc + 1) + el] = carry + incl - v;
+            }
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+        if (c == 0 && s == 0 && lane == 0) a.expert_prefix[(int64_t)d * (a.E_loc + 1) + a.E_loc] = carry;
     }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += kThreads)
+        running[e] += a.ws_expert[((int64_t)s * a.C + c) * a.E + e];
     const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
     const int lt = threadIdx.x;
     for (int base = t0; base < t1; base += sub) {   // block-uniform trip count
-        for (int i = threadIdx.x; i < a.E * W; i += kThreads) mask[i] = 0u;
+        for (int i = threadIdx.x; i < a.E * WS; i += kThreads) mask[i] = 0u;
         __syncthreads();
         const int t = base + lt;
         const bool mine = lt < sub && t < t1;
         const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t) * a.k;
-        if (mine)
-            for (int j = 0; j < a.k; ++j) {
-                const int64_t e = row[j];
-                if (e >= 0 && e < a.E) atomicOr(&mask[e * W + (lt >> 5)], 1u << (lt & 31));
-            }
+        // The token's ids are loaded in batches of 8 before any shared-memory atomic.
+        for (int j0 = 0; j0 < a.k; j0 += 8) {
+            int64_t ev[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ev[i] = (mine && j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (ev[i] >= 0 && ev[i] < a.E) atomicOr(&mask[ev[i] * WS + (lt >> 5)], 1u << (lt & 31));
+        }
         __syncthreads();
-        if (mine)
-            for (int j = 0; j < a.k; ++j) {
-                const int64_t e = row[j];
+        for (int j0 = 0; j0 < a.k; j0 += 8) {
+            int64_t ev[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ev[i] = (mine && j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (!mine || j0 + i >= a.k) continue;
+                const int64_t e = ev[i];
                 int r = -1;
                 if (e >= 0 && e < a.E) {
-                    const uint32_t* m = mask + e * W;
+                    const uint32_t* m = mask + e * WS;
                     r = running[e];
                     for (int w = 0; w < (lt >> 5); ++w) r += __popc(m[w]);
                     r += __popc(m[lt >> 5] & ((1u << (lt & 31)) - 1u));
                 }
-                a.expert_rows[((int64_t)s * a.T + t) * a.k + j] = r;
+                a.expert_rows[((int64_t)s * a.T + t) * a.k + j0 + i] = r;
             }
+        }
         __syncthreads();
         for (int e = threadIdx.x; e < a.E; e += kThreads) {
             int add = 0;
-            for (int w = 0; w < W; ++w) add += __popc(mask[e * W + w]);
+            for (int w = 0; w < W; ++w) add += __popc(mask[e * WS + w]);
             running[e] += add;
         }
         __syncthreads();
@@ -367,7 +386,8 @@ extern "C" {
 size_t ep_layout_workspace_size(const ep_shape* sh) {
     if (ep::check_shape(sh) != EP_OK) return 0;
     return ep::ws_cnt_bytes(sh) +
-           (size_t)sh->num_ranks * sh->num_channels * sh->num_experts * sizeof(int32_t);
+           (size_t)sh->num_ranks * sh->num_channels * sh->num_experts * sizeof(int32_t) +
+           (size_t)sh->num_experts * sizeof(int32_t);
 }
 
 ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* layout,
@@ -423,9 +443,10 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     a.num_recv_per_expert = handle->num_recv_tokens_per_expert;
     a.ws_cnt = reinterpret_cast<int32_t*>(workspace);
     a.ws_expert = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(workspace) + ws_cnt_bytes(sh));
+    a.ws_etot = a.ws_expert + (size_t)a.R * a.C * a.E;
     a.expert_rows = handle->expert_rows;
     a.expert_prefix = handle->expert_prefix;
-    // Bitmask words per expert: at most 6144 words (24 KB) of shared memory.
+    // Bitmask words per expert (rows padded to an odd stride): at most ~6144 + E words.
     a.ew = expert ? (a.E >= 6144 ? 1 : (6144 / a.E > 16 ? 16 : 6144 / a.E)) : 1;
     a.err = launch->error_flags;
 
@@ -436,11 +457,11 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     if (e == cudaSuccess)
         e = launch_pdl(layout_prefix_kernel, grid, dim3(kThreads), 0, launch->stream, a);
     if (e == cudaSuccess && expert)
-        e = launch_pdl(layout_expert_scan_kernel, dim3(a.R), dim3(kThreads), sizeof(int) * (size_t)a.E_loc,
+        e = launch_pdl(layout_expert_scan_kernel, dim3((unsigned)ceil_div(a.E, kWarps)), dim3(kThreads), 0,
                        launch->stream, a);
     if (e == cudaSuccess && expert)
         e = launch_pdl(layout_expert_rows_kernel, grid, dim3(kThreads),
-                       sizeof(uint32_t) * (size_t)a.E * (1 + (size_t)a.ew), launch->stream, a);
+                       sizeof(uint32_t) * (size_t)a.E * (1 + (size_t)(a.ew | 1)), launch->stream, a);
     if (e != cudaSuccess) return cuda_fail(e);
     return end_call(launch);
 }

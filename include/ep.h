@@ -263,7 +263,7 @@ EP_API ep_status ep_get_layout(const ep_shape* shape, const int64_t* topk_idx, e
  *   - The scratch is a file-scope device array of EP_LAYOUT_STATIC_SCRATCH_BYTES bytes
  *     inside libep.so; every GPU that loads the library holds it until the process
  *     exits. Shapes whose ep_layout_workspace_size exceeds it return
- *     EP_ERR_UNSUPPORTED before anything is enqueued (R=8, C=12, E=256 needs ~96 KiB).
+ *     EP_ERR_UNSUPPORTED before anything is enqueued (R=8, C=12, E=256 needs ~97 KiB).
  *   - The first call on a device (with that device current) looks up the array's
  *     device address; make that first call before any stream capture.
  *   - The call itself allocates nothing and frees nothing.

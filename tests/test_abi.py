@@ -49,7 +49,7 @@ def test_workspace_size_formula_and_limits(ep):
     sh = ep.make_shape(8, 4096, 7168, 256, 8, C=12)
     ws = ep.ep_layout_workspace_size(sh)
     cnt = (8 * 8 * 12 * 4 + 255) // 256 * 256
-    assert ws == cnt + 8 * 12 * 256 * 4
+    assert ws == cnt + 8 * 12 * 256 * 4 + 256 * 4
     assert ep.ep_layout_workspace_size(ep.make_shape(65, 16, 128, 65, 1)) == 0     # R > 64
     assert ep.ep_layout_workspace_size(ep.make_shape(8, 16, 100, 64, 2)) == 0      # H % 128
     assert ep.ep_layout_workspace_size(ep.make_shape(3, 16, 128, 8, 2)) == 0       # E % R

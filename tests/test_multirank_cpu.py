@@ -63,3 +63,11 @@ def test_bytes_model_counts_each_byte_once():
         8 * 4096 * (8 * 12 + 8 * 4) + 173_000 * (8 * 12 + 4)
     assert b["combine"] - (173_000 * 7168 * 2 + 8 * 4096 * 7168 * 2) == \
         8 * 4096 * 8 * 4 + 8 * 4096 * 8 * 12
+
+
+def test_every_bench_workload_resolves():
+    sys.path.insert(0, ROOT)
+    import bench
+    for name in bench.WORKLOAD_TEXT:
+        w = bench.workload_config(name)
+        assert w.E % w.R == 0 and w.H % 128 == 0
