@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCombineU = 1;        // units per thread per batch in the LL combine
+constexpr int kScanPre = 4;         // earlier entries per thread loaded up front (send)
 
 __device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
 
@@ -114,6 +115,17 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
             if (u < cunits) pre[i] = ld_stream_v4(src + (int64_t)u * 16);
         }
     }
+    // The source's earlier entries (for the slot ranks) do not depend on this token
+    // either: each thread loads its first kScanPre of them now, with the row and the
+    // token's own ids, so all three share one memory round trip.
+    const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
+    const int lim = t * a.k + a.k;
+    int64_t pre_e[kScanPre];
+#pragma unroll
+    for (int q = 0; q < kScanPre; ++q) {
+        const int i = threadIdx.x + q * kThreads;
+        pre_e[q] = i < lim ? __ldg(tk + i) : -1;
+    }
     if (threadIdx.x < a.k) {
         s_e[threadIdx.x] = a.topk_idx[tok * a.k + threadIdx.x];
         s_cnt[threadIdx.x] = 0;
@@ -121,10 +133,15 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     __syncthreads();
 
     // Rank of each entry among the source's earlier entries with the same expert.
-    const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
-    const int lim = t * a.k + a.k;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < lim; i += kThreads) {
+#pragma unroll
+    for (int q = 0; q < kScanPre; ++q) {
+        const int i = threadIdx.x + q * kThreads;
+        const int64_t e = pre_e[q];
+        if (e < 0) continue;
+        for (int j = 0; j < a.k; ++j)
+            if (e == s_e[j] && i < t * a.k + j) atomicAdd(&s_cnt[j], 1);
+    }
+    for (int i = threadIdx.x + kScanPre * kThreads; i < lim; i += kThreads) {
         const int64_t e = __ldg(tk + i);
         if (e < 0) continue;
         for (int j = 0; j < a.k; ++j)
