@@ -178,42 +178,144 @@ def reduce_max(v: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def run_e2e(world, dev, stream, step, x, topk, wts, out, total_bytes, e2e_steps):
-    """The same step through the same C-ABI calls with host buffers: pinned host ->
-    device copies of x / topk_idx / topk_weights and a device -> host copy of the
-    combined output inside every timed step."""
+def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
+    """The dsv3 step through the same C-ABI calls with host buffers: every step copies its
+    inputs (x, topk_idx, topk_weights) from pinned host memory to the device and its result
+    (the combined output) back to pinned host memory.
+
+    Measured two ways: serial (copy in, compute, copy out on one stream) and pipelined as a
+    user would run consecutive steps -- input copies, kernels and output copies on three
+    streams with double-buffered device inputs and outputs, so step i+1's input copy and
+    step i-1's output copy overlap step i's kernels (the two copy directions are
+    independent). `value` is the pipelined figure."""
     import torch
-    x_h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-    x_h.copy_(x)
-    topk_h = torch.empty(topk.shape, dtype=topk.dtype, pin_memory=True)
-    topk_h.copy_(topk)
-    wts_h = torch.empty(wts.shape, dtype=wts.dtype, pin_memory=True)
-    wts_h.copy_(wts)
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    w = plan["w"]
+    R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
+    sh = ep.make_shape(R, T, H, E, k, C)
+    lb, rb = plan["keep"][0], plan["keep"][1]
+    from combine_layout_02_gb300.buffers import worst_case_row_offsets
+    off = worst_case_row_offsets(R, T)
+    x0, topk0, wts0, out0 = plan["x"], plan["topk"], plan["wts"], plan["out"]
+    x_h = torch.empty(x0.shape, dtype=x0.dtype, pin_memory=True)
+    x_h.copy_(x0)
+    topk_h = torch.empty(topk0.shape, dtype=topk0.dtype, pin_memory=True)
+    topk_h.copy_(topk0)
+    wts_h = torch.empty(wts0.shape, dtype=wts0.dtype, pin_memory=True)
+    wts_h.copy_(wts0)
+    out_h = [torch.empty(out0.shape, dtype=out0.dtype, pin_memory=True) for _ in range(2)]
+    x_d = [x0, torch.empty_like(x0)]
+    topk_d = [topk0, torch.empty_like(topk0)]
+    wts_d = [wts0, torch.empty_like(wts0)]
+    out_d = [out0, torch.empty_like(out0)]
+    layout_s, handle = lb.layout(), lb.handle(rb.recv_src_idx)
 
-    def e2e_step():
-        x.copy_(x_h, non_blocking=True)
-        topk.copy_(topk_h, non_blocking=True)
-        wts.copy_(wts_h, non_blocking=True)
-        step()
-        out_h.copy_(out, non_blocking=True)
+    def kernels(b, stream):
+        launch = ep.make_launch(stream, error_flags=err)
+        ep.ep_get_layout(sh, topk_d[b], layout_s, handle, lb.workspace, launch)
+        ep.ep_dispatch(sh, x_d[b], ep.EP_BF16, None, ep.EP_BF16, topk_d[b], wts_d[b], handle,
+                       rb.recv_x, None, rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx,
+                       off, launch)
+        ep.ep_combine(sh, rb.recv_x, off, handle, ep.EP_COMBINE_WEIGHTED, topk_d[b], wts_d[b],
+                      None, out_d[b], None, launch)
 
-    e2e_step()
+    # serial: one stream, copy in -> kernels -> copy out
+    cur = torch.cuda.current_stream()
+
+    def serial_step():
+        x_d[0].copy_(x_h, non_blocking=True)
+        topk_d[0].copy_(topk_h, non_blocking=True)
+        wts_d[0].copy_(wts_h, non_blocking=True)
+        kernels(0, cur)
+        out_h[0].copy_(out_d[0], non_blocking=True)
+
+    serial_step()
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(cur)
     for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+        serial_step()
+    e1.record(cur)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    serial_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    # pipelined: input copies, kernels and output copies on their own streams,
+    # double-buffered device inputs / outputs
+    nc = max(1, copy_streams)
+    s_in = [torch.cuda.Stream() for _ in range(nc)]
+    s_out = [torch.cuda.Stream() for _ in range(nc)]
+    s_comp = torch.cuda.Stream()
+    ev_in = [[torch.cuda.Event() for _ in range(nc)] for _ in range(2)]
+    ev_comp = [torch.cuda.Event(), torch.cuda.Event()]
+    ev_out = [[torch.cuda.Event() for _ in range(nc)] for _ in range(2)]
+    xh_parts = list(torch.chunk(x_h.view(-1, H), nc))
+    oh_parts = [list(torch.chunk(o.view(-1, H), nc)) for o in out_h]
+    xd_parts = [list(torch.chunk(xd.view(-1, H), nc)) for xd in x_d]
+    od_parts = [list(torch.chunk(od.view(-1, H), nc)) for od in out_d]
+
+    def issue(i):
+        b = i & 1
+        for c in range(nc):
+            with torch.cuda.stream(s_in[c]):
+                if i >= 2:
+                    s_in[c].wait_event(ev_comp[b])   # step i-2 has finished reading inputs b
+                xd_parts[b][c].copy_(xh_parts[c], non_blocking=True)
+                if c == 0:
+                    topk_d[b].copy_(topk_h, non_blocking=True)
+                    wts_d[b].copy_(wts_h, non_blocking=True)
+                ev_in[b][c].record(s_in[c])
+            s_comp.wait_event(ev_in[b][c])
+            if i >= 2:
+                s_comp.wait_event(ev_out[b][c])      # step i-2's output b has left the device
+        kernels(b, s_comp)
+        ev_comp[b].record(s_comp)
+        for c in range(nc):
+            with torch.cuda.stream(s_out[c]):
+                s_out[c].wait_event(ev_comp[b])
+                oh_parts[b][c].copy_(od_parts[b][c], non_blocking=True)
+                ev_out[b][c].record(s_out[c])
+
+    for i in range(4):
+        issue(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(s_in[0])
+    for i in range(e2e_steps):
+        issue(i)
+    for bb in range(2):
+        for c in range(nc):
+            s_in[0].wait_event(ev_out[bb][c])
+    p1.record(s_in[0])
+    torch.cuda.synchronize()
+    pipe_ms = reduce_max(p0.elapsed_time(p1) / e2e_steps, world, dev)
+
     h2d = x_h.numel() * x_h.element_size() + topk_h.numel() * 8 + wts_h.numel() * 4
-    d2h = out_h.numel() * out_h.element_size()
-    return {"value": round(world * total_bytes / (e2e_ms * 1e6), 1), "unit": "GB/s",
-            "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+    d2h = out_h[0].numel() * out_h[0].element_size()
+
+    # raw pinned-copy bandwidth of the link, each direction alone (context for the above)
+    def copy_gbs(dst, src, nbytes):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dst.copy_(src, non_blocking=True)
+        a.record(cur)
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        b.record(cur)
+        torch.cuda.synchronize()
+        return round(3 * nbytes / (a.elapsed_time(b) * 1e6), 1)
+
+    link = {"h2d_gbs": copy_gbs(x_d[0], x_h, x_h.numel() * 2),
+            "d2h_gbs": copy_gbs(out_h[0], out_d[0], d2h)}
+    return {"value": round(world * total_bytes / (pipe_ms * 1e6), 1), "unit": "GB/s",
+            "ms_per_step": round(pipe_ms, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "mode": f"pipelined: input copies and output copies ({nc} streams each) and "
+                    "kernels on their own streams, double-buffered device inputs/outputs",
+            "serial_ms_per_step": round(serial_ms, 4),
+            "serial_value": round(world * total_bytes / (serial_ms * 1e6), 1),
+            "link": link}
 
 
 PHASE_KERNEL = {"dispatch": "dispatch_kernel<copy>", "dispatch_fp8": "dispatch_kernel<quant>",
@@ -505,8 +607,8 @@ def run_ours(args, rank, world):
 
     e2e = None
     if args.workload == "dsv3" and not args.no_e2e:
-        e2e = run_e2e(world, dev, stream, step, plan["x"], plan["topk"], plan["wts"], plan["out"],
-                      total_bytes, max(3, min(args.steps, 20)))
+        e2e = run_e2e(world, dev, plan, ep, err, total_bytes, max(4, min(args.steps, 20)),
+                      args.e2e_copy_streams)
 
     peak, peak_kind = measured_peaks()
     w = plan["w"]
@@ -624,6 +726,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
+    ap.add_argument("--e2e-copy-streams", type=int, default=1,
+                    help="streams per copy direction in the pipelined end-to-end measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="dsv3",
                     help="dsv3 is the benchmark line; the others are extra measurements")
     ap.add_argument("--nmax", type=int, default=0,
