@@ -40,7 +40,7 @@ def lib():
         L.oracle_dispatch.restype = I64
         L.oracle_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, P, P]
         L.oracle_combine.restype = I64
-        L.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P]
+        L.oracle_ll_dispatch.argtypes = [I, I, I, I, I, I, I, I, I, F, P, P, P, P, P, P, P, P]
         L.oracle_ll_dispatch.restype = I64
         L.oracle_ll_combine.argtypes = [I, I, I, I, I, I, P, P, P, P, P]
         L.oracle_ll_combine.restype = None
@@ -207,8 +207,9 @@ def combine(y: np.ndarray, send_head: np.ndarray, row_offset: np.ndarray, E: int
 
 def ll_dispatch(x: np.ndarray, topk_idx: np.ndarray, E: int, nmax: int, use_fp8: bool,
                 fill_x: int = 0, fill_src: int = -7, scale_mode: int = SCALE_FP32,
-                tensor_scale: float = 0.0) -> dict:
-    """Low-latency dispatch into fixed per-(expert, source) slots."""
+                tensor_scale: float = 0.0, packed: bool = False) -> dict:
+    """Low-latency dispatch into fixed per-(expert, source) slots, or (packed) into
+    per-expert rows without gaps between the sources."""
     x = _c(x, np.uint16)
     topk_idx = _c(topk_idx, np.int64)
     R, T, H = x.shape
@@ -227,7 +228,8 @@ def ll_dispatch(x: np.ndarray, topk_idx: np.ndarray, E: int, nmax: int, use_fp8:
         "layout_range": np.empty((R, E_loc, R, 2), np.int32),
     }
     bad = lib().oracle_ll_dispatch(
-        R, T, H, E, k, nmax, int(bool(use_fp8)), scale_mode, tensor_scale, _p(x), _p(topk_idx),
+        R, T, H, E, k, nmax, int(bool(use_fp8)), int(bool(packed)), scale_mode, tensor_scale,
+        _p(x), _p(topk_idx),
         _p(res["recv_x"]),
         _p(res["recv_x_scales"]), _p(res["src_info"]), _p(res["slot"]),
         _p(res["recv_expert_count"]), _p(res["layout_range"]))

@@ -477,10 +477,16 @@ EXPORT int64_t oracle_combine(int R, int T, int H, int E, int k, int mode,
  * the port notes the UE8M0 format for these kernels), src_info[d][el][pos] = t, slot[s][t][j] = pos (-1 when masked),
  * recv_expert_count[d][el] = sum_s count, layout_range[d][el][s] = (s*nmax, count).
  * Counts are int32 (the port returns int32 counts and handles).
+ *
+ * packed != 0: the same rows without gaps between the source sub-slots (the packed
+ * variant of the "specific format" for a grouped GEMM): expert e's rows are numbered
+ * 0, 1, 2, ... over all sources in (s, t) order, so source s starts at the sum of the
+ * counts of sources s' < s; layout_range[d][el][s] = (that start, count). The per-source
+ * capacity check (count <= nmax) is the same in both layouts.
  * Returns the number of entries skipped (outside [0, E), or beyond nmax).
  */
 EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, int use_fp8,
-                                  int scale_mode, float tensor_scale,
+                                  int packed, int scale_mode, float tensor_scale,
                                   const uint16_t* x, const int64_t* topk_idx,
                                   void* recv_x, void* recv_x_scales, int32_t* src_info,
                                   int32_t* slot, int32_t* recv_expert_count,
@@ -493,6 +499,7 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
     const size_t scale_elem = scale_mode == 2 ? 1 : 4;
     int64_t bad = 0;
     int32_t* run = (int32_t*)malloc(sizeof(int32_t) * (size_t)(E + 1));
+    int32_t* next_row = (int32_t*)calloc((size_t)(E + 1), sizeof(int32_t));  /* packed */
     uint8_t* qrow = (uint8_t*)malloc((size_t)H + 1);
     float* srow = (float*)malloc(sizeof(float) * (size_t)(G + 1));
     uint8_t* brow = (uint8_t*)malloc((size_t)G + 1);
@@ -500,6 +507,10 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
     memset(recv_expert_count, 0, sizeof(int32_t) * (size_t)E);
     for (int s = 0; s < R; s++) {
         for (int e = 0; e < E; e++) run[e] = 0;
+        for (int e = 0; e < E; e++) {      /* where source s starts in each expert region */
+            int d = e / E_loc, el = e % E_loc;
+            layout_range[(((int64_t)d * E_loc + el) * R + s) * 2] = packed ? next_row[e] : s * nmax;
+        }
         for (int t = 0; t < T; t++) {
             const int64_t tok = (int64_t)s * T + t;
             const uint16_t* xrow = x + tok * H;
@@ -510,8 +521,9 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
                 if (e == -1) continue;
                 if (e < 0 || e >= E || run[e] >= nmax) { bad++; continue; }
                 int d = (int)(e / E_loc), el = (int)(e % E_loc);
-                int32_t pos = s * nmax + run[e];
+                int32_t pos = packed ? next_row[e] : s * nmax + run[e];
                 run[e] += 1;
+                next_row[e] += 1;
                 int64_t dst = ((int64_t)d * E_loc + el) * slots + pos;
                 if (use_fp8) {
                     memcpy((uint8_t*)recv_x + (size_t)dst * H, qrow, (size_t)H);
@@ -527,12 +539,12 @@ EXPORT int64_t oracle_ll_dispatch(int R, int T, int H, int E, int k, int nmax, i
         for (int e = 0; e < E; e++) {
             int d = e / E_loc, el = e % E_loc;
             int64_t lr = (((int64_t)d * E_loc + el) * R + s) * 2;
-            layout_range[lr + 0] = s * nmax;
             layout_range[lr + 1] = run[e];
             recv_expert_count[d * E_loc + el] += run[e];
         }
     }
     free(run);
+    free(next_row);
     free(qrow);
     free(srow);
     free(brow);

@@ -129,3 +129,96 @@ def test_ll_capacity_overflow_is_reported():
     assert res["bad_entries"] == 2 * 6
     assert np.all(res["slot"][:, 4:] == -1)
     np.testing.assert_array_equal(res["recv_expert_count"][0], [8, 0])
+
+
+def _golden_ll():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "ll_hand_example.json")) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_hand_example(packed):
+    g = _golden_ll()
+    R, T, E, k, nmax = g["R"], g["T"], g["E"], g["k"], g["nmax"]
+    topk = np.array(g["topk_idx"], np.int64)
+    x = (np.arange(R * T * 128, dtype=np.uint16) % 7919).reshape(R, T, 128)
+    res = oracle.ll_dispatch(x, topk, E, nmax, False, packed=packed)
+    pre = "packed_" if packed else ""
+    assert res["bad_entries"] == 0
+    np.testing.assert_array_equal(res["slot"], g[pre + "slot"])
+    np.testing.assert_array_equal(res["layout_range"], g[pre + "layout_range"])
+    np.testing.assert_array_equal(res["recv_expert_count"], g["recv_expert_count"])
+    E_loc = E // R
+    for e in range(E):
+        d, el = divmod(e, E_loc)
+        want = g[pre + "src_info"][f"e{e}"]
+        items = enumerate(want) if packed else ((int(p), t) for p, t in want.items())
+        for pos, t in items:
+            assert res["src_info"][d, el, pos] == t
+
+
+def test_ll_packed_is_the_gapless_compaction_of_the_slot_layout():
+    """The packed layout, checked three independent ways: (1) each expert's region is
+    the concatenation over sources of the slot layout's filled sub-slots; (2) a source's
+    start is the running sum of the earlier sources' counts (numpy cumsum); (3) the
+    position of each entry is its rank among the expert's entries sorted by (source,
+    token), which is also the expert-major placement's row minus the expert's start."""
+    w, inp = _case(R=4, T=24, H=256, E=16, k=4, nmax=30, mask_p=0.1, seed=45)
+    R, T, E, k, nmax = w.R, w.T, w.E, w.k, w.nmax
+    E_loc = E // R
+    topk = inp["topk_idx"]
+    for use_fp8 in (False, True):
+        sl = oracle.ll_dispatch(inp["x"], topk, E, nmax, use_fp8)
+        pk = oracle.ll_dispatch(inp["x"], topk, E, nmax, use_fp8, packed=True)
+        assert pk["bad_entries"] == 0
+        np.testing.assert_array_equal(pk["recv_expert_count"], sl["recv_expert_count"])
+        cnt = sl["layout_range"][..., 1]                       # [R][E_loc][R]
+        np.testing.assert_array_equal(pk["layout_range"][..., 1], cnt)
+        starts = np.concatenate([np.zeros(cnt.shape[:-1] + (1,), cnt.dtype),
+                                 np.cumsum(cnt, -1)[..., :-1]], -1)
+        np.testing.assert_array_equal(pk["layout_range"][..., 0], starts)
+        for d in range(R):
+            for el in range(E_loc):
+                n = int(pk["recv_expert_count"][d, el])
+                keys = ["recv_x", "src_info"] + (["recv_x_scales"] if use_fp8 else [])
+                for key in keys:
+                    parts = [sl[key][d, el, s * nmax: s * nmax + cnt[d, el, s]] for s in range(R)]
+                    np.testing.assert_array_equal(pk[key][d, el, :n], np.concatenate(parts))
+    ranks = {}
+    for e in range(E):
+        entries = sorted((s, t) for s in range(R) for t in range(T) if e in topk[s, t])
+        for i, st in enumerate(entries):
+            ranks[(e,) + st] = i
+    em = oracle.expert_layout(topk, E)
+    for s in range(R):
+        for t in range(T):
+            for j in range(k):
+                e = int(topk[s, t, j])
+                if e < 0:
+                    assert pk["slot"][s, t, j] == -1
+                    continue
+                d, el = divmod(e, E_loc)
+                assert pk["slot"][s, t, j] == ranks[(e, s, t)]
+                assert pk["slot"][s, t, j] == em["expert_rows"][s, t, j] - em["expert_prefix"][d, el]
+
+
+def test_ll_packed_combine_equals_slot_layout_combine():
+    w, inp = _case(R=4, T=16, H=256, E=16, k=4, nmax=16, mask_p=0.1, seed=46)
+    E_loc = w.E // w.R
+    sl = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, False)
+    pk = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, False, packed=True)
+    # the same expert outputs, placed by each layout's slots
+    rng = np.random.default_rng(47)
+    ys = np.zeros_like(sl["recv_x"])
+    yp = np.zeros_like(pk["recv_x"])
+    topk = inp["topk_idx"]
+    for s, t, j in zip(*np.nonzero(topk >= 0)):
+        d, el = divmod(int(topk[s, t, j]), E_loc)
+        row = (rng.standard_normal(w.H).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        ys[d, el, sl["slot"][s, t, j]] = row
+        yp[d, el, pk["slot"][s, t, j]] = row
+    a = oracle.ll_combine(ys, topk, inp["topk_weights"], sl["slot"], w.E, w.nmax)
+    b = oracle.ll_combine(yp, topk, inp["topk_weights"], pk["slot"], w.E, w.nmax)
+    np.testing.assert_array_equal(a, b)
