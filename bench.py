@@ -337,13 +337,16 @@ WORKLOAD_TEXT = {
     "dsv3_expert_major": "dsv3 shape; layout with the expert-major placement + expert-major bf16 "
                          "dispatch (one row per token-expert entry, grouped per local expert) + "
                          "weighted combine; worst-case regions R*T*min(k, E_loc) rows per rank",
+    "ll_decode_packed": "ll_decode with the packed receive layout (no gaps between the sources' "
+                        "rows of an expert; send phase = per-source count kernel + send kernel)",
 }
+BASE_WORKLOAD = {"dsv3_expert_major": "dsv3", "ll_decode_packed": "ll_decode"}
 
 
 def workload_config(name: str):
-    """The synthetic workload behind a bench workload name (the expert-major measurement
-    runs on the dsv3 workload)."""
-    return workloads.CONFIGS["dsv3" if name == "dsv3_expert_major" else name]
+    """The synthetic workload behind a bench workload name (the expert-major and packed
+    low-latency measurements run on the dsv3 / ll_decode workloads)."""
+    return workloads.CONFIGS[BASE_WORKLOAD.get(name, name)]
 
 
 def make_plan(args, ep, dev, stream, launch):
@@ -460,10 +463,11 @@ def make_plan(args, ep, dev, stream, launch):
                     "dispatch_em": Tt * H * 2 + M * H * 2 + Tt * k * (8 + 4 + 4) + M * (4 + 4),
                     "combine_em": M * H * 2 + Tt * H * 2 + Tt * k * (8 + 4 + 4)}, M
         plan["nbytes"] = nbytes
-    elif args.workload == "ll_decode":
+    elif args.workload in ("ll_decode", "ll_decode_packed"):
         sh = ep.make_shape(R, T, H, E, k, C, nmax=w.nmax)
-        buf = LLBuffers(sh, True, device=dev)
-        ybuf = LLBuffers(sh, False, device=dev)
+        packed = args.workload == "ll_decode_packed"
+        buf = LLBuffers(sh, True, device=dev, packed=packed)
+        ybuf = LLBuffers(sh, False, device=dev, packed=packed)
         ep.ep_ll_dispatch(sh, x, topk, False, ep.EP_PHASE_BOTH, ybuf.struct(), launch)
         out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
         s_buf, s_y = buf.struct(), ybuf.struct()
@@ -631,7 +635,7 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: " + WORKLOAD_TEXT[args.workload].format(T=w.T),
                    "R": w.R, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "C": w.C,
-                   "valid_entries" if args.workload in ("ll_decode", "dsv3_expert_major") else "recv_rows": units,
+                   "valid_entries" if args.workload in ("ll_decode", "ll_decode_packed", "dsv3_expert_major") else "recv_rows": units,
                    "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)",
                    "l2": plan["l2"]},
     }

@@ -39,6 +39,7 @@ EP_BF16, EP_FP8_E4M3 = 0, 1
 EP_COMBINE_SUM, EP_COMBINE_WEIGHTED = 0, 1
 EP_PHASE_SEND, EP_PHASE_RECV, EP_PHASE_BOTH = 1, 2, 3
 EP_FP8_SCALE_FP32, EP_FP8_SCALE_POW2, EP_FP8_SCALE_UE8M0, EP_FP8_SCALE_TENSOR = 0, 1, 2, 3
+EP_LL_LAYOUT_SLOTS, EP_LL_LAYOUT_PACKED = 0, 1
 EP_MAX_RANKS = 64
 
 # Every function include/ep.h declares (checked by the ABI test).
@@ -100,7 +101,7 @@ class ep_recv(ctypes.Structure):
 class ep_ll_buffer(ctypes.Structure):
     _fields_ = [("recv_x", _P), ("recv_x_scales", _P), ("src_info", _P), ("slot", _P),
                 ("send_count", _P), ("recv_expert_count", _P), ("layout_range", _P),
-                ("fp8", ep_fp8_options)]
+                ("fp8", ep_fp8_options), ("layout", _I32)]
 
 
 _lib = None

@@ -9,7 +9,8 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (EP_BF16, EP_FP8_E4M3, EP_FP8_SCALE_FP32, EP_FP8_SCALE_UE8M0, ep_fp8_options,
+from . import (EP_BF16, EP_FP8_E4M3, EP_FP8_SCALE_FP32, EP_FP8_SCALE_UE8M0, EP_LL_LAYOUT_PACKED,
+               EP_LL_LAYOUT_SLOTS, ep_fp8_options,
                ep_handle, ep_layout, ep_layout_workspace_size, ep_ll_buffer, ep_shape, _ptr)
 
 
@@ -93,7 +94,8 @@ class LLBuffers:
     """Low-latency receive buffers and handle for one shape."""
 
     def __init__(self, shape: ep_shape, use_fp8: bool, device="cuda", fill: Optional[int] = None,
-                 fp8_scale: int = EP_FP8_SCALE_FP32, tensor_scale: float = 0.0):
+                 fp8_scale: int = EP_FP8_SCALE_FP32, tensor_scale: float = 0.0,
+                 packed: bool = False):
         R, T, H, E, k = (shape.num_ranks, shape.num_tokens, shape.hidden, shape.num_experts,
                          shape.num_topk)
         nmax = shape.num_max_dispatch_tokens_per_rank
@@ -101,6 +103,7 @@ class LLBuffers:
         slots = R * nmax
         i32 = dict(dtype=torch.int32, device=device)
         self.fp8 = ep_fp8_options(fp8_scale, tensor_scale)
+        self.layout = EP_LL_LAYOUT_PACKED if packed else EP_LL_LAYOUT_SLOTS
         if use_fp8:
             self.recv_x = torch.empty((R, E_loc, slots, H), dtype=torch.uint8, device=device)
             sdt = torch.uint8 if fp8_scale == EP_FP8_SCALE_UE8M0 else torch.float32
@@ -120,7 +123,7 @@ class LLBuffers:
     def struct(self) -> ep_ll_buffer:
         return ep_ll_buffer(_ptr(self.recv_x), _ptr(self.recv_x_scales), _ptr(self.src_info),
                             _ptr(self.slot), _ptr(self.send_count), _ptr(self.recv_expert_count),
-                            _ptr(self.layout_range), self.fp8)
+                            _ptr(self.layout_range), self.fp8, self.layout)
 
 
 def compact_row_offsets(counts: Sequence[int]) -> list:

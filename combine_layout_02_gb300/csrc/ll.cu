@@ -19,6 +19,13 @@
 // entries (at most Nmax*k of them), so no block waits on another. Extra blocks write
 // the per-(destination, expert, source) count signals; the receive kernel only
 // reads those signals.
+//
+// Packed variant (no gaps between the sources): entry (t, j) of source s takes
+//   sum over s' < s of count[s'][e] + (the same in-source rank),
+// so the per-source counts must exist before any row is placed. A small kernel with
+// one block per source writes them (as the count signals) and lets the send kernel
+// start at once; the send kernel loads its row and ranks its entries, then waits for
+// the counts (programmatic dependent launch) before it writes anything.
 #include "rowops.cuh"
 
 namespace ep {
@@ -43,11 +50,32 @@ struct LLArgs {
     int32_t* layout_range;
     const char* y;
     char* out;
-    int R, T, H, E, k, E_loc, nmax, use_fp8, write_recv;
+    int R, T, H, E, k, E_loc, nmax, use_fp8, write_recv, packed;
     int col_split;                  // combine: blocks per token (column ranges)
     QuantMode qm;                   // send phase with use_fp8: scale format
     uint32_t* err;
 };
+
+// Packed layout, first kernel: block s counts source s's entries per expert (capped at
+// Nmax, as the send kernel caps them) into send_count[e][s]. It lets the send kernel
+// launch immediately: that kernel reads nothing of this one's before its own wait.
+__global__ void __launch_bounds__(kThreads) ll_count_kernel(LLArgs a) {
+    extern __shared__ int hist[];   // [E]
+    const int s = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    for (int i = threadIdx.x; i < a.E; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < a.T * a.k; i += kThreads) {
+        const int64_t e = __ldg(tk + i);
+        if (e >= 0 && e < a.E) atomicAdd(&hist[(int)e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < a.E; e += kThreads)
+        a.send_count[(int64_t)e * a.R + s] = min(hist[e], a.nmax);
+}
 
 // Blocks [0, R*T): one per source token. Blocks [R*T, R*T + R): the count signals of
 // one destination rank d (sent by every source to d). When the receive phase runs in
@@ -61,8 +89,26 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     extern __shared__ int hist[];   // [R][E_loc], count blocks only
     const int b = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
-    pdl_wait();
+    if (!a.packed) pdl_wait();
 
+    if (b >= a.R * a.T && a.packed) {
+        // Receive outputs of destination d from the count kernel's signals.
+        const int d = b - a.R * a.T;
+        pdl_wait();
+        for (int el = threadIdx.x; el < a.E_loc; el += kThreads) {
+            const int64_t e = (int64_t)d * a.E_loc + el;
+            int start = 0;
+            for (int src = 0; src < a.R; ++src) {
+                const int c = a.send_count[e * a.R + src];
+                a.layout_range[(e * a.R + src) * 2 + 0] = start;
+                a.layout_range[(e * a.R + src) * 2 + 1] = c;
+                start += c;
+            }
+            a.recv_expert_count[e] = start;
+        }
+        pdl_trigger();
+        return;
+    }
     if (b >= a.R * a.T) {
         const int d = b - a.R * a.T;
         const int lo = d * a.E_loc;
@@ -148,6 +194,8 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
             if (e == s_e[j] && i < t * a.k + j) atomicAdd(&s_cnt[j], 1);
     }
     __syncthreads();
+    // Packed: the earlier sources' counts come from the count kernel.
+    if (a.packed) pdl_wait();
 
     if (threadIdx.x < a.k) {
         const int j = threadIdx.x;
@@ -161,7 +209,12 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
                 raise_flag(a.err, EP_DEVERR_SLOT_OVERFLOW);
             } else {
                 const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
-                pos = s * a.nmax + s_cnt[j];
+                int start = s * a.nmax;
+                if (a.packed) {
+                    start = 0;
+                    for (int src = 0; src < s; ++src) start += a.send_count[e * a.R + src];
+                }
+                pos = start + s_cnt[j];
                 row = ((int64_t)d * a.E_loc + el) * slots + pos;
                 a.src_info[row] = t;
             }
@@ -218,9 +271,9 @@ __global__ void __launch_bounds__(kThreads) ll_recv_kernel(LLArgs a) {
     int total = 0;
     for (int s = 0; s < a.R; ++s) {
         const int c = a.send_count[(int64_t)e * a.R + s];
-        total += c;
-        a.layout_range[((int64_t)e * a.R + s) * 2 + 0] = s * a.nmax;
+        a.layout_range[((int64_t)e * a.R + s) * 2 + 0] = a.packed ? total : s * a.nmax;
         a.layout_range[((int64_t)e * a.R + s) * 2 + 1] = c;
+        total += c;
     }
     a.recv_expert_count[e] = total;
 }
@@ -306,6 +359,7 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     }
     if ((phase & EP_PHASE_RECV) && (buf->recv_expert_count == nullptr || buf->layout_range == nullptr))
         return EP_ERR_INVALID_ARG;
+    if (buf->layout != EP_LL_LAYOUT_SLOTS && buf->layout != EP_LL_LAYOUT_PACKED) return EP_ERR_INVALID_ARG;
 
     LLArgs a{};
     a.x = reinterpret_cast<const char*>(x);
@@ -326,13 +380,24 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     a.nmax = sh->num_max_dispatch_tokens_per_rank;
     a.use_fp8 = use_fp8 ? 1 : 0;
     a.write_recv = (phase & EP_PHASE_RECV) ? 1 : 0;
+    a.packed = buf->layout == EP_LL_LAYOUT_PACKED ? 1 : 0;
     a.qm.mode = buf->fp8.scale_format;
     a.qm.tscale = buf->fp8.tensor_scale;
     a.qm.tinv = a.qm.mode == EP_FP8_SCALE_TENSOR ? 1.0f / buf->fp8.tensor_scale : 0.0f;
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;
-    if (phase & EP_PHASE_SEND) {
+    if ((phase & EP_PHASE_SEND) && a.packed) {
+        cudaError_t e = launch_pdl(ll_count_kernel, dim3((unsigned)a.R), dim3(kThreads),
+                                   sizeof(int) * (size_t)a.E, launch->stream, a);
+        if (e == cudaSuccess) {
+            // Token blocks, plus one receive-output block per destination with BOTH.
+            const unsigned blocks = (unsigned)(a.R * a.T + (a.write_recv ? a.R : 0));
+            if (blocks > 0)
+                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+    } else if (phase & EP_PHASE_SEND) {
         const unsigned blocks = (unsigned)(a.R * a.T + a.R);
         cudaError_t e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads),
                                    sizeof(int) * (size_t)a.E, launch->stream, a);

@@ -206,10 +206,19 @@ typedef struct ep_recv {
     ep_fp8_options fp8;
 } ep_recv;
 
+/* Placement of the low-latency receive rows inside each expert's R*Nmax slots.
+ *   EP_LL_LAYOUT_SLOTS   source s owns slots [s*Nmax, (s+1)*Nmax), filled in token
+ *                        order (gaps after each source's count) [default]
+ *   EP_LL_LAYOUT_PACKED  no gaps: the expert's rows are 0 .. recv_expert_count-1 in
+ *                        (source, token) order, source s starting at the sum of the
+ *                        counts of sources s' < s, so a grouped GEMM reads one
+ *                        contiguous block per expert. The send phase then takes two
+ *                        kernels (a per-source count, then the rows). */
+typedef enum ep_ll_layout { EP_LL_LAYOUT_SLOTS = 0, EP_LL_LAYOUT_PACKED = 1 } ep_ll_layout;
+
 /* Low-latency buffers and handle ([README] low-latency example; [HOOK]). All dev.
  * Reading of the pages' "specific format for a grouped GEMM": rank d holds, per local
- * expert el, R*Nmax fixed slots; source s owns slots [s*Nmax, (s+1)*Nmax), filled in
- * token order.
+ * expert el, R*Nmax slots, placed as `layout` says (see ep_ll_layout).
  *   recv_x            [R][E_loc][R*Nmax][H] e4m3 (use_fp8) or bf16
  *   recv_x_scales     [R][E_loc][R*Nmax][H/128] fp32, or uint8 with
  *                     EP_FP8_SCALE_UE8M0 (use_fp8 only)
@@ -220,6 +229,8 @@ typedef struct ep_recv {
  *   recv_expert_count [R][E_loc] int32 (int32 as in the port)
  *   layout_range      [R][E_loc][R][2] int32: (first slot, count) per source
  *   fp8               scale format when use_fp8 (see ep_fp8_scale)
+ *   layout            ep_ll_layout (0 = EP_LL_LAYOUT_SLOTS); the combine reads the
+ *                     slot array, so it serves both layouts unchanged
  * Slots beyond each count are left unwritten (stale data of earlier calls). */
 typedef struct ep_ll_buffer {
     void* recv_x;
@@ -230,6 +241,7 @@ typedef struct ep_ll_buffer {
     int32_t* recv_expert_count;
     int32_t* layout_range;
     ep_fp8_options fp8;
+    int32_t layout;
 } ep_ll_buffer;
 
 /* ---------------------------------------------------------------- layout */

@@ -84,8 +84,9 @@ class GpuRun:
         return out, cw
 
     def ll_dispatch(self, use_fp8: bool, phase=ep.EP_PHASE_BOTH, buf: LLBuffers = None,
-                    fp8_scale=ep.EP_FP8_SCALE_FP32, tensor_scale=0.0) -> LLBuffers:
-        buf = buf or LLBuffers(self.sh, use_fp8, fill=0x5A, fp8_scale=fp8_scale, tensor_scale=tensor_scale)
+                    fp8_scale=ep.EP_FP8_SCALE_FP32, tensor_scale=0.0, packed=False) -> LLBuffers:
+        buf = buf or LLBuffers(self.sh, use_fp8, fill=0x5A, fp8_scale=fp8_scale, tensor_scale=tensor_scale,
+                               packed=packed)
         ep.ep_ll_dispatch(self.sh, self.x, self.topk, use_fp8, phase, buf.struct(), self.launch)
         return buf
 

@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(ep):
 
 
 def test_host_only_helpers(ep):
-    assert ep.ep_abi_version() == 100
+    assert ep.ep_abi_version() == 101
     assert ep.ep_kernel_launch_count() >= 0
     assert ep.lib().ep_status_string(1).startswith(b"EP_ERR_INVALID_ARG")
     assert ep.lib().ep_last_cuda_error() == b""
@@ -111,6 +111,11 @@ def test_invalid_arguments_rejected_on_host(ep):
     st = L.ep_ll_dispatch(ctypes.byref(sh_ll2), 0x7000, 0x8000, 0, ep.EP_PHASE_SEND,
                           ctypes.byref(buf_b), ctypes.byref(launch))
     assert st == ep.EP_ERR_INVALID_ARG        # a scale format needs use_fp8
+    buf_l = ep.ep_ll_buffer(0x1000, None, 0x2000, 0x3000, 0x4000, 0x5000, 0x6000,
+                            ep.ep_fp8_options(0, 0.0), 2)
+    st = L.ep_ll_dispatch(ctypes.byref(sh_ll2), 0x7000, 0x8000, 0, ep.EP_PHASE_SEND,
+                          ctypes.byref(buf_l), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG        # unknown receive layout
     # unsupported shape
     big = ep.make_shape(65, 4, 128, 65, 1)
     st = L.ep_dispatch(ctypes.byref(big), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,

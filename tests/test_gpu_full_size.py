@@ -133,11 +133,13 @@ def test_group_limited_fp8_full_size():
     assert run.flags() == 0
 
 
-def test_ll_decode_full_size():
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_decode_full_size(packed):
     w, inp, run = _run("ll_decode")
-    buf = run.ll_dispatch(True, phase=ep.EP_PHASE_SEND)
+    buf = run.ll_dispatch(True, phase=ep.EP_PHASE_SEND, packed=packed)
     run.ll_dispatch(True, phase=ep.EP_PHASE_RECV, buf=buf)
-    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, True, fill_x=0x5A)
+    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, True, fill_x=0x5A,
+                             packed=packed)
     for key in ("slot", "recv_expert_count", "layout_range", "src_info"):
         np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
     filled = exp["src_info"] != -7
@@ -147,9 +149,9 @@ def test_ll_decode_full_size():
     np.testing.assert_array_equal(got_q, exp["recv_x"][filled])
     np.testing.assert_array_equal(got_s.view(np.uint32), exp["recv_x_scales"][filled].view(np.uint32))
     # bf16 slots + weighted LL combine of identity experts, against the oracle pipeline
-    b16 = run.ll_dispatch(False)
+    b16 = run.ll_dispatch(False, packed=packed)
     out = run.ll_combine(b16.recv_x, b16)
-    e16 = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, False)
+    e16 = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, False, packed=packed)
     ref = oracle.ll_combine(e16["recv_x"], inp["topk_idx"], inp["topk_weights"], e16["slot"],
                             w.E, w.nmax)
     assert_close_bf16(host_bits(out), ref)

@@ -131,15 +131,16 @@ def test_normal_step_cuda_graph_replay():
     assert int(err.item()) == 0
 
 
-def test_low_latency_step_cuda_graph_replay():
+@pytest.mark.parametrize("packed", [False, True])
+def test_low_latency_step_cuda_graph_replay(packed):
     w = workloads.Workload("llg", R=8, T=96, H=1024, E=64, k=8, nmax=128, mask_p=0.05, seed=210)
     inp = workloads.make_workload(w)
     sh = ep.make_shape(w.R, w.T, w.H, w.E, w.k, 1, nmax=w.nmax)
     topk = torch.from_numpy(inp["topk_idx"]).cuda()
     wts = torch.from_numpy(inp["topk_weights"]).cuda()
     x = dev_bf16(inp["x"])
-    buf = LLBuffers(sh, use_fp8=True)
-    ybuf = LLBuffers(sh, use_fp8=False)
+    buf = LLBuffers(sh, use_fp8=True, packed=packed)
+    ybuf = LLBuffers(sh, use_fp8=False, packed=packed)
     out = torch.empty((w.R, w.T, w.H), dtype=torch.bfloat16, device="cuda")
 
     def step(stream):
@@ -167,12 +168,12 @@ def test_low_latency_step_cuda_graph_replay():
         wts.copy_(torch.from_numpy(inp2["topk_weights"]))
         g.replay()
         torch.cuda.synchronize()
-        exp = oracle.ll_dispatch(inp2["x"], inp2["topk_idx"], w.E, w.nmax, True)
+        exp = oracle.ll_dispatch(inp2["x"], inp2["topk_idx"], w.E, w.nmax, True, packed=packed)
         for key in ("slot", "recv_expert_count", "layout_range"):
             np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
         filled = exp["src_info"] != -7
         np.testing.assert_array_equal(host_bits(buf.recv_x)[filled], exp["recv_x"][filled])
-        e16 = oracle.ll_dispatch(inp2["x"], inp2["topk_idx"], w.E, w.nmax, False)
+        e16 = oracle.ll_dispatch(inp2["x"], inp2["topk_idx"], w.E, w.nmax, False, packed=packed)
         cexp = oracle.ll_combine(e16["recv_x"], inp2["topk_idx"], inp2["topk_weights"], e16["slot"],
                                  w.E, w.nmax)
         assert_close_bf16(host_bits(out), cexp)

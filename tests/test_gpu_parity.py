@@ -223,10 +223,12 @@ def _ll_setup(name):
 
 @pytest.mark.parametrize("name", list(LL_CASES))
 @pytest.mark.parametrize("use_fp8", [False, True])
-def test_ll_dispatch_bit_exact(name, use_fp8):
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_dispatch_bit_exact(name, use_fp8, packed):
     w, inp, run = _ll_setup(name)
-    buf = run.ll_dispatch(use_fp8)
-    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, use_fp8, fill_x=0x5A5A if not use_fp8 else 0x5A)
+    buf = run.ll_dispatch(use_fp8, packed=packed)
+    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, use_fp8, packed=packed,
+                             fill_x=0x5A5A if not use_fp8 else 0x5A)
     for key in ("slot", "recv_expert_count", "layout_range", "src_info"):
         np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
     np.testing.assert_array_equal(host_bits(buf.recv_x), exp["recv_x"])
@@ -238,10 +240,11 @@ def test_ll_dispatch_bit_exact(name, use_fp8):
 
 
 @pytest.mark.parametrize("name", list(LL_CASES))
-def test_ll_phase_split_equals_single_call(name):
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_phase_split_equals_single_call(name, packed):
     w, inp, run = _ll_setup(name)
-    both = run.ll_dispatch(True)
-    split = run.ll_dispatch(True, phase=ep.EP_PHASE_SEND)
+    both = run.ll_dispatch(True, packed=packed)
+    split = run.ll_dispatch(True, phase=ep.EP_PHASE_SEND, packed=packed)
     torch.cuda.synchronize()
     run.ll_dispatch(True, phase=ep.EP_PHASE_RECV, buf=split)
     for key in ("recv_x", "recv_x_scales", "src_info", "slot", "send_count", "recv_expert_count",
@@ -255,9 +258,10 @@ def test_ll_phase_split_equals_single_call(name):
 
 
 @pytest.mark.parametrize("name", list(LL_CASES))
-def test_ll_combine_within_tolerance(name):
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_combine_within_tolerance(name, packed):
     w, inp, run = _ll_setup(name)
-    buf = run.ll_dispatch(False)
+    buf = run.ll_dispatch(False, packed=packed)
     rng = np.random.default_rng(w.seed + 3000)
     y32 = rng.standard_normal(tuple(buf.recv_x.shape)).astype(np.float32)
     yb = torch.from_numpy(y32).to(torch.bfloat16)
@@ -273,7 +277,8 @@ def test_ll_combine_within_tolerance(name):
     del out_send
 
 
-def test_ll_slot_overflow_flag():
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_slot_overflow_flag(packed):
     """Duplicate experts in a token push a (source, expert) count past Nmax: flagged and
     skipped exactly like the oracle, no fault."""
     R, T, H, E, k, nmax = 2, 4, 128, 4, 2, 4
@@ -282,12 +287,13 @@ def test_ll_slot_overflow_flag():
     inp = {"x": workloads.make_hidden(rng, R, T, H), "topk_idx": topk,
            "topk_weights": np.full((R, T, k), 0.5, np.float32)}
     run = GpuRun(R, T, H, E, k, 1, inp, nmax=nmax)
-    buf = run.ll_dispatch(False)
+    buf = run.ll_dispatch(False, packed=packed)
     assert run.flags() & ep.EP_DEVERR_SLOT_OVERFLOW
-    exp = oracle.ll_dispatch(inp["x"], topk, E, nmax, False)
+    exp = oracle.ll_dispatch(inp["x"], topk, E, nmax, False, packed=packed)
     assert exp["bad_entries"] == 2 * 4
     np.testing.assert_array_equal(host_bits(buf.slot), exp["slot"])
     np.testing.assert_array_equal(host_bits(buf.recv_expert_count), exp["recv_expert_count"])
+    np.testing.assert_array_equal(host_bits(buf.layout_range), exp["layout_range"])
 
 
 # ----------------------------------------------------------------------------- FP8 scale modes
@@ -343,11 +349,12 @@ def test_fp8_scale_modes_extreme_values(mode, ts):
 
 
 @pytest.mark.parametrize("mode,ts", MODES)
-def test_ll_dispatch_scale_modes_bit_exact(mode, ts):
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_dispatch_scale_modes_bit_exact(mode, ts, packed):
     w, inp, run = _ll_setup("masked")
-    buf = run.ll_dispatch(True, fp8_scale=mode, tensor_scale=ts)
+    buf = run.ll_dispatch(True, fp8_scale=mode, tensor_scale=ts, packed=packed)
     exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, True, fill_x=0x5A,
-                             scale_mode=mode, tensor_scale=ts)
+                             scale_mode=mode, tensor_scale=ts, packed=packed)
     np.testing.assert_array_equal(host_bits(buf.recv_x), exp["recv_x"])
     filled = exp["src_info"] != -7
     _cmp_scales(host_bits(buf.recv_x_scales)[filled], exp["recv_x_scales"][filled], mode)
