@@ -41,6 +41,8 @@ EP_PHASE_SEND, EP_PHASE_RECV, EP_PHASE_BOTH = 1, 2, 3
 EP_FP8_SCALE_FP32, EP_FP8_SCALE_POW2, EP_FP8_SCALE_UE8M0, EP_FP8_SCALE_TENSOR = 0, 1, 2, 3
 EP_LL_LAYOUT_SLOTS, EP_LL_LAYOUT_PACKED = 0, 1
 EP_MAX_RANKS = 64
+EP_MAX_TOPK = 32
+EP_EXPERT_MAJOR_MAX_EXPERTS = 4096
 
 # Every function include/ep.h declares (checked by the ABI test).
 EXPORTED_SYMBOLS = (

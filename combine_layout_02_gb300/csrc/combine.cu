@@ -115,16 +115,22 @@ extern "C" ep_status ep_combine(const ep_shape* sh, const void* y, const int64_t
     if (st != EP_OK) return st;
     if (handle == nullptr || launch == nullptr) return EP_ERR_INVALID_ARG;
     const int64_t ntok = (int64_t)sh->num_ranks * sh->num_tokens;
+    CombineArgs a{};
+    if ((st = load_row_offsets(y_row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
+    // With no row in any region nothing is read from y / recv_topk_weights (every token
+    // gets +0 and zero weight sums), so those may be NULL.
+    const bool rows = a.off.v[sh->num_ranks] > a.off.v[0];
     if (ntok > 0 && handle->send_head == nullptr) return EP_ERR_INVALID_ARG;
-    if (ntok > 0 && (y == nullptr || out == nullptr)) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && (out == nullptr || (rows && y == nullptr))) return EP_ERR_INVALID_ARG;
     if (mode != EP_COMBINE_SUM && mode != EP_COMBINE_WEIGHTED) return EP_ERR_INVALID_ARG;
     if (mode == EP_COMBINE_WEIGHTED && ntok > 0 && (topk_idx == nullptr || topk_weights == nullptr))
         return EP_ERR_INVALID_ARG;
-    if ((combined_topk_weights == nullptr) != (recv_topk_weights == nullptr)) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && recv_topk_weights != nullptr && combined_topk_weights == nullptr)
+        return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && rows && combined_topk_weights != nullptr && recv_topk_weights == nullptr)
+        return EP_ERR_INVALID_ARG;
     if (((uintptr_t)y & 15) != 0 || ((uintptr_t)out & 15) != 0) return EP_ERR_INVALID_ARG;
 
-    CombineArgs a{};
-    if ((st = load_row_offsets(y_row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
     a.y = reinterpret_cast<const char*>(y);
     a.send_head = handle->send_head;
     a.topk_idx = topk_idx;

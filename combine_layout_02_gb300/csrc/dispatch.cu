@@ -145,20 +145,27 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     if (st != EP_OK) return st;
     if (handle == nullptr || out == nullptr || launch == nullptr) return EP_ERR_INVALID_ARG;
     const int64_t ntok = (int64_t)sh->num_ranks * sh->num_tokens;
+    DispatchArgs a{};
+    if ((st = load_row_offsets(out->row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
+    // Receive buffers may be NULL when the regions hold no row at all (nothing is
+    // written then; tokens that had a destination raise EP_DEVERR_RECV_OVERFLOW).
+    const bool rows = a.off.v[sh->num_ranks] > a.off.v[0];
     if (ntok > 0 && handle->send_head == nullptr) return EP_ERR_INVALID_ARG;
-    if (ntok > 0 && (x == nullptr || out->recv_x == nullptr)) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && x == nullptr) return EP_ERR_INVALID_ARG;
+    if (rows && out->recv_x == nullptr) return EP_ERR_INVALID_ARG;
     if (x_dtype == EP_FP8_E4M3 && recv_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
     if (x_dtype != EP_BF16 && x_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
     if (recv_dtype != EP_BF16 && recv_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
-    if (recv_dtype == EP_FP8_E4M3 && out->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
+    if (recv_dtype == EP_FP8_E4M3 && rows && out->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
     if (x_dtype == EP_FP8_E4M3 && ntok > 0 && x_scales == nullptr) return EP_ERR_INVALID_ARG;
     // Handle reuse passes no topk (the pages assert this); topk outputs then cannot be
     // produced. A first dispatch passes topk_idx and gets recv_topk_idx.
-    if (topk_idx == nullptr && (topk_weights != nullptr || out->recv_topk_idx != nullptr ||
-                                out->recv_topk_weights != nullptr))
+    // (With no token there is nothing to check: empty arrays may come as NULL.)
+    if (ntok > 0 && topk_idx == nullptr && (topk_weights != nullptr || out->recv_topk_idx != nullptr ||
+                                            out->recv_topk_weights != nullptr))
         return EP_ERR_INVALID_ARG;
-    if (topk_idx != nullptr && out->recv_topk_idx == nullptr) return EP_ERR_INVALID_ARG;
-    if (topk_weights == nullptr && out->recv_topk_weights != nullptr) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && topk_idx != nullptr && rows && out->recv_topk_idx == nullptr) return EP_ERR_INVALID_ARG;
+    if (ntok > 0 && topk_weights == nullptr && out->recv_topk_weights != nullptr) return EP_ERR_INVALID_ARG;
     // 16-byte vector access of rows.
     if (((uintptr_t)x & 15) != 0 || ((uintptr_t)out->recv_x & 15) != 0) return EP_ERR_INVALID_ARG;
     // Scale formats other than per-group fp32 apply to a fused quantisation only.
@@ -170,8 +177,6 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
         !(out->fp8.tensor_scale > 0.0f && out->fp8.tensor_scale <= 3.4028234e38f))
         return EP_ERR_INVALID_ARG;
 
-    DispatchArgs a{};
-    if ((st = load_row_offsets(out->row_offset, sh->num_ranks, &a.off)) != EP_OK) return st;
     a.x = reinterpret_cast<const char*>(x);
     a.x_scales = x_scales;
     a.topk_idx = topk_idx;

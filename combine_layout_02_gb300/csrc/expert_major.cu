@@ -143,10 +143,13 @@ ep_status ep_dispatch_expert_major(const ep_shape* sh, const void* x, ep_dtype r
     ep_status st = em_common(sh, handle, topk_idx, out->row_offset, launch, &a);
     if (st != EP_OK) return st;
     if (recv_dtype != EP_BF16 && recv_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
-    if (a.ntok > 0 && (x == nullptr || out->recv_x == nullptr)) return EP_ERR_INVALID_ARG;
+    // Receive buffers may be NULL when the regions hold no row (nothing is written).
+    const bool rows = a.off.v[a.R] > a.off.v[0];
+    if (a.ntok > 0 && x == nullptr) return EP_ERR_INVALID_ARG;
+    if (rows && out->recv_x == nullptr) return EP_ERR_INVALID_ARG;
     if (out->recv_topk_idx != nullptr) return EP_ERR_INVALID_ARG;   // one entry per row
-    if (out->recv_topk_weights != nullptr && topk_weights == nullptr) return EP_ERR_INVALID_ARG;
-    if (recv_dtype == EP_FP8_E4M3 && out->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
+    if (a.ntok > 0 && out->recv_topk_weights != nullptr && topk_weights == nullptr) return EP_ERR_INVALID_ARG;
+    if (recv_dtype == EP_FP8_E4M3 && rows && out->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
     if (((uintptr_t)x & 15) != 0 || ((uintptr_t)out->recv_x & 15) != 0) return EP_ERR_INVALID_ARG;
     const int fmt = out->fp8.scale_format;
     if (fmt < EP_FP8_SCALE_FP32 || fmt > EP_FP8_SCALE_TENSOR) return EP_ERR_INVALID_ARG;
@@ -183,7 +186,8 @@ ep_status ep_combine_expert_major(const ep_shape* sh, const void* y, const int64
     ep_status st = em_common(sh, handle, topk_idx, y_row_offset, launch, &a);
     if (st != EP_OK) return st;
     if (mode != EP_COMBINE_SUM && mode != EP_COMBINE_WEIGHTED) return EP_ERR_INVALID_ARG;
-    if (a.ntok > 0 && (y == nullptr || out == nullptr)) return EP_ERR_INVALID_ARG;
+    const bool rows = a.off.v[a.R] > a.off.v[0];     // no row: y is never read
+    if (a.ntok > 0 && (out == nullptr || (rows && y == nullptr))) return EP_ERR_INVALID_ARG;
     if (mode == EP_COMBINE_WEIGHTED && a.ntok > 0 && topk_weights == nullptr) return EP_ERR_INVALID_ARG;
     if (((uintptr_t)y & 15) != 0 || ((uintptr_t)out & 15) != 0) return EP_ERR_INVALID_ARG;
     a.y = reinterpret_cast<const char*>(y);

@@ -345,10 +345,11 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
         return EP_ERR_INVALID_ARG;
     if (buf->send_count == nullptr) return EP_ERR_INVALID_ARG;
     if (phase & EP_PHASE_SEND) {
-        if (buf->recv_x == nullptr || buf->src_info == nullptr || buf->slot == nullptr)
+        if (buf->recv_x == nullptr || buf->src_info == nullptr ||
+            (sh->num_tokens > 0 && buf->slot == nullptr))
             return EP_ERR_INVALID_ARG;
         if (sh->num_tokens > 0 && (x == nullptr || topk_idx == nullptr)) return EP_ERR_INVALID_ARG;
-        if (use_fp8 && buf->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
+        if (use_fp8 && sh->num_tokens > 0 && buf->recv_x_scales == nullptr) return EP_ERR_INVALID_ARG;
         const int fmt = buf->fp8.scale_format;
         if (fmt < EP_FP8_SCALE_FP32 || fmt > EP_FP8_SCALE_TENSOR) return EP_ERR_INVALID_ARG;
         if (fmt != EP_FP8_SCALE_FP32 && !use_fp8) return EP_ERR_INVALID_ARG;
@@ -422,7 +423,7 @@ ep_status ep_ll_combine(const ep_shape* sh, const void* y, const int64_t* topk_i
     if (st != EP_OK) return st;
     if ((phase & EP_PHASE_BOTH) == 0 || (phase & ~EP_PHASE_BOTH) != 0) return EP_ERR_INVALID_ARG;
     if (phase & EP_PHASE_RECV) {
-        if (handle == nullptr || handle->slot == nullptr) return EP_ERR_INVALID_ARG;
+        if (handle == nullptr || (sh->num_tokens > 0 && handle->slot == nullptr)) return EP_ERR_INVALID_ARG;
         if (sh->num_tokens > 0 && (y == nullptr || topk_idx == nullptr || topk_weights == nullptr || out == nullptr))
             return EP_ERR_INVALID_ARG;
         if (((uintptr_t)y & 15) != 0 || ((uintptr_t)out & 15) != 0) return EP_ERR_INVALID_ARG;

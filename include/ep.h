@@ -195,7 +195,10 @@ typedef struct ep_handle {
  *                     when topk_idx and topk_weights are given.
  *   recv_src_idx      dev [rows] int32 (nullable): token index of each row.
  *   fp8               scale format of a fused quantisation (bf16 x, e4m3 receive);
- *                     must be EP_FP8_SCALE_FP32 for other dtype combinations. */
+ *                     must be EP_FP8_SCALE_FP32 for other dtype combinations.
+ * When the regions hold no row at all (row_offset[R] == row_offset[0]) nothing is
+ * written and the row arrays may be NULL; the same holds for y and recv_topk_weights
+ * of a combine over empty regions. */
 typedef struct ep_recv {
     void* recv_x;
     void* recv_x_scales;

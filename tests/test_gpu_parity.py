@@ -359,3 +359,27 @@ def test_ll_dispatch_scale_modes_bit_exact(mode, ts, packed):
     filled = exp["src_info"] != -7
     _cmp_scales(host_bits(buf.recv_x_scales)[filled], exp["recv_x_scales"][filled], mode)
     np.testing.assert_array_equal(host_bits(buf.slot), exp["slot"])
+
+
+def test_all_entries_masked_empty_regions():
+    """Every entry masked: exact regions hold no row, so the receive arrays are empty
+    (NULL pointers) and the calls must still succeed; combine gives +0 everywhere."""
+    R, T, H, E, k, C = 4, 33, 256, 8, 3, 5
+    rng = np.random.default_rng(114)
+    inp = {"x": workloads.make_hidden(rng, R, T, H), "topk_idx": np.full((R, T, k), -1, np.int64),
+           "topk_weights": np.zeros((R, T, k), np.float32)}
+    run = GpuRun(R, T, H, E, k, C, inp)
+    ref = oracle.layout(inp["topk_idx"], E, C)
+    got = run.layout()
+    for key, arr in got.items():
+        np.testing.assert_array_equal(arr, ref[key], err_msg=key)
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    assert off[-1] == 0
+    run.dispatch(off)
+    run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, with_topk=False)
+    y = torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    out, cw = run.combine(y, off, ep.EP_COMBINE_WEIGHTED,
+                          recv_topk_weights=torch.empty((0, k), device="cuda"))
+    assert torch.count_nonzero(out.view(torch.int16)) == 0
+    assert torch.count_nonzero(cw) == 0
+    assert run.flags() == 0
