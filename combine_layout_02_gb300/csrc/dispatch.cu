@@ -45,7 +45,7 @@ struct DispatchArgs {
 };
 
 template <int MODE, int U>
-__global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
     __shared__ int s_dst[kWarps][EP_MAX_RANKS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -56,6 +56,11 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
 
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
         const int t = (int)(g % a.T);
+        const char* src = a.x + g * (int64_t)a.H * a.in_elem;
+        // Quantising: the row's first batch does not depend on the metadata, so its load
+        // shares the metadata's memory round trip.
+        uint4 qa[U], qb[U];
+        if (MODE == kQuant) quant_load<U>(src, a.H >> 4, 0, lane, 32, qa, qb);
 
         // Destination rows in ascending rank order.
         int nd = 0;
@@ -99,7 +104,6 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
         }
 
         // Payload.
-        const char* src = a.x + g * (int64_t)a.H * a.in_elem;
         if (MODE == kCopy) {
             scatter_copy_row<U>(src, a.recv_x, s_row[warp], nd, out_row_bytes, lane, 32);
             if (a.copy_scales) {
@@ -109,8 +113,8 @@ __global__ void __launch_bounds__(kThreads) dispatch_kernel(DispatchArgs a) {
                     for (int i = lane; i < G; i += 32) rs[s_row[warp][p] * G + i] = ss[i];
             }
         } else {
-            scatter_quant_row<U>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
-                                 s_row[warp], nd, a.H, a.qm, lane, 32);
+            scatter_quant_row_loaded<U>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
+                                        s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
         }
         __syncwarp();
     }

@@ -73,6 +73,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_em_kernel(EmArgs a) {
     pdl_wait();
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
         const int t = (int)(g % a.T);
+        const char* src = a.x + g * (int64_t)a.H * 2;
+        uint4 qa[kQuantU], qb[kQuantU];   // quantising: first batch loaded with the metadata
+        if (QUANT) quant_load<kQuantU>(src, a.H >> 4, 0, lane, 32, qa, qb);
         const int nd = entry_rows(a, g, lane, s_row[warp], s_coef[warp]);
         __syncwarp();
         if (lane < nd) {
@@ -80,10 +83,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_em_kernel(EmArgs a) {
             if (a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
             if (a.recv_weights != nullptr) a.recv_weights[row] = s_coef[warp][lane];
         }
-        const char* src = a.x + g * (int64_t)a.H * 2;
         if (QUANT)
-            scatter_quant_row<kQuantU>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
-                                       s_row[warp], nd, a.H, a.qm, lane, 32);
+            scatter_quant_row_loaded<kQuantU>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
+                                              s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
         else
             scatter_copy_row<kCopyU>(src, a.recv_x, s_row[warp], nd, (int64_t)a.H * 2, lane, 32);
         __syncwarp();

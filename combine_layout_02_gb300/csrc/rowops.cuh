@@ -123,27 +123,39 @@ __device__ __forceinline__ void store_quant_unit(uint8_t* __restrict__ q_base, v
     }
 }
 
+// Loads batch u0 of a row for quantisation: units u0 + i*stride + first (i < U), as two
+// 16-byte halves each; zero beyond the row (those lanes still take part in the shuffles).
 template <int U>
-__device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
-                                                  uint8_t* __restrict__ q_base,
-                                                  void* __restrict__ s_base,
-                                                  const int64_t* rows, int nd, int H,
-                                                  const QuantMode& qm, int first, int stride,
-                                                  int u_start = 0) {
+__device__ __forceinline__ void quant_load(const char* __restrict__ src, int units, int u0, int first,
+                                           int stride, uint4 (&a)[U], uint4 (&b)[U]) {
+#pragma unroll
+    for (int i = 0; i < U; ++i) {
+        const int u = u0 + i * stride + first;
+        if (u < units) {
+            a[i] = ld_stream_v4(src + (int64_t)u * 32);
+            b[i] = ld_stream_v4(src + (int64_t)u * 32 + 16);
+        } else {
+            a[i] = make_uint4(0, 0, 0, 0);
+            b[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+}
+
+// Quantises one row and stores it to every destination row, software-pipelined: (a, b)
+// hold the batch at u_start, already loaded (the caller can issue that load before its
+// own metadata loads), and each next batch is loaded before the current one is
+// quantised and stored, so two batches per thread are in flight.
+template <int U>
+__device__ __forceinline__ void scatter_quant_row_loaded(const char* __restrict__ src,
+                                                         uint8_t* __restrict__ q_base,
+                                                         void* __restrict__ s_base,
+                                                         const int64_t* rows, int nd, int H,
+                                                         const QuantMode& qm, int first, int stride,
+                                                         int u_start, uint4 (&a)[U], uint4 (&b)[U]) {
     const int units = H >> 4;
     for (int u0 = u_start; u0 < units; u0 += stride * U) {
-        uint4 a[U], b[U];
-#pragma unroll
-        for (int i = 0; i < U; ++i) {
-            const int u = u0 + i * stride + first;
-            if (u < units) {
-                a[i] = ld_stream_v4(src + (int64_t)u * 32);
-                b[i] = ld_stream_v4(src + (int64_t)u * 32 + 16);
-            } else {
-                a[i] = make_uint4(0, 0, 0, 0);
-                b[i] = make_uint4(0, 0, 0, 0);
-            }
-        }
+        uint4 na[U], nb[U];
+        quant_load<U>(src, units, u0 + stride * U, first, stride, na, nb);
 #pragma unroll
         for (int i = 0; i < U; ++i) {
             const int u = u0 + i * stride + first;
@@ -152,7 +164,24 @@ __device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
             const uint4 q = quant_unit(a[i], b[i], qm, scale, sbyte);
             if (u < units) store_quant_unit(q_base, s_base, rows, nd, H, u, q, scale, sbyte, qm.mode);
         }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            a[i] = na[i];
+            b[i] = nb[i];
+        }
     }
+}
+
+template <int U>
+__device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
+                                                  uint8_t* __restrict__ q_base,
+                                                  void* __restrict__ s_base,
+                                                  const int64_t* rows, int nd, int H,
+                                                  const QuantMode& qm, int first, int stride,
+                                                  int u_start = 0) {
+    uint4 a[U], b[U];
+    quant_load<U>(src, H >> 4, u_start, first, stride, a, b);
+    scatter_quant_row_loaded<U>(src, q_base, s_base, rows, nd, H, qm, first, stride, u_start, a, b);
 }
 
 // out = sum_p coef[p] * rows[p], fp32 accumulation in registers, one bf16 RNE store.
