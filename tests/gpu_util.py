@@ -46,8 +46,8 @@ class GpuRun:
         self.R, self.T, self.H, self.E, self.k, self.C = R, T, H, E, k, C
         self.sh = ep.make_shape(R, T, H, E, k, C, nmax=nmax)
         self.inp = inp
-        self.topk = torch.from_numpy(inp["topk_idx"]).cuda()
-        self.wts = torch.from_numpy(inp["topk_weights"]).cuda()
+        self.topk = torch.from_numpy(np.ascontiguousarray(inp["topk_idx"])).cuda()
+        self.wts = torch.from_numpy(np.ascontiguousarray(inp["topk_weights"])).cuda()
         self.x = dev_bf16(inp["x"]) if inp.get("x") is not None else None
         self.err = torch.zeros(1, dtype=torch.int32, device="cuda")
         self.launch = ep.make_launch(error_flags=self.err)
