@@ -2,7 +2,7 @@
 
 Each .cu file is compiled to an object in parallel, then linked into
 ``combine_layout_02_gb300/_build/libep.so``. The CUDA runtime is linked statically, so
-the library only needs the NVIDIA kernel-mode driver (libcuda) at run time.
+the library only needs the CUDA driver library (libcuda) at run time.
 """
 from __future__ import annotations
 
