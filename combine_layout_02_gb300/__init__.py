@@ -27,6 +27,7 @@ __all__ = [
     "EpError", "ep_shape", "ep_launch", "ep_layout", "ep_handle", "ep_recv", "ep_ll_buffer",
     "lib", "library_path", "make_shape", "make_launch",
     "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
+    "ep_buffer_size_hint", "ep_size_hint",
     "ep_dispatch", "ep_combine", "ep_dispatch_expert_major", "ep_combine_expert_major",
     "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
     "ep_read_error_flags_sync", "ep_kernel_launch_count", "ep_abi_version",
@@ -47,6 +48,7 @@ EP_EXPERT_MAJOR_MAX_EXPERTS = 4096
 # Every function include/ep.h declares (checked by the ABI test).
 EXPORTED_SYMBOLS = (
     "ep_layout_workspace_size", "ep_get_layout", "ep_get_layout_static_scratch",
+    "ep_buffer_size_hint",
     "ep_dispatch", "ep_combine", "ep_dispatch_expert_major", "ep_combine_expert_major",
     "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
     "ep_read_error_flags_sync", "ep_status_string", "ep_last_cuda_error",
@@ -106,6 +108,15 @@ class ep_ll_buffer(ctypes.Structure):
                 ("fp8", ep_fp8_options), ("layout", _I32)]
 
 
+class ep_size_hint(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64 if n.endswith("_rows") else ctypes.c_uint64) for n in (
+        "recv_rows", "recv_x_bytes", "recv_x_scales_bytes", "recv_topk_idx_bytes",
+        "recv_topk_weights_bytes", "recv_src_idx_bytes", "expert_major_rows",
+        "expert_major_x_bytes", "ll_slots", "ll_recv_x_bytes", "ll_recv_x_scales_bytes",
+        "ll_src_info_bytes", "ll_slot_bytes", "ll_send_count_bytes", "ll_recv_expert_count_bytes",
+        "ll_layout_range_bytes", "layout_workspace_bytes")]
+
+
 _lib = None
 
 
@@ -122,6 +133,8 @@ def lib():
         S = ctypes.POINTER
         L.ep_layout_workspace_size.argtypes = [S(ep_shape)]
         L.ep_layout_workspace_size.restype = ctypes.c_size_t
+        L.ep_buffer_size_hint.argtypes = [S(ep_shape), ctypes.c_int, _I32, S(ep_size_hint)]
+        L.ep_buffer_size_hint.restype = ctypes.c_int
         L.ep_get_layout.argtypes = [S(ep_shape), _P, S(ep_layout), S(ep_handle), _P,
                                     ctypes.c_size_t, S(ep_launch)]
         L.ep_get_layout_static_scratch.argtypes = [S(ep_shape), _P, S(ep_layout), S(ep_handle),
@@ -214,6 +227,15 @@ def _launch(launch) -> ep_launch:
 
 def ep_layout_workspace_size(shape: ep_shape) -> int:
     return int(lib().ep_layout_workspace_size(ctypes.byref(shape)))
+
+
+def ep_buffer_size_hint(shape: ep_shape, recv_dtype: int = EP_BF16,
+                        fp8_scale: int = EP_FP8_SCALE_FP32) -> dict:
+    """Worst-case buffer sizes for `shape` (see ep_size_hint in ep.h) as a dict."""
+    h = ep_size_hint()
+    _check("ep_buffer_size_hint",
+           lib().ep_buffer_size_hint(ctypes.byref(shape), recv_dtype, fp8_scale, ctypes.byref(h)))
+    return {name: int(getattr(h, name)) for name, _ in ep_size_hint._fields_}
 
 
 def ep_get_layout(shape: ep_shape, topk_idx, layout: Optional[ep_layout], handle: ep_handle,

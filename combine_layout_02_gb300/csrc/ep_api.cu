@@ -117,6 +117,53 @@ ep_status ep_read_error_flags_sync(const uint32_t* error_flags, uint32_t* host_f
     return EP_OK;
 }
 
+ep_status ep_buffer_size_hint(const ep_shape* sh, ep_dtype recv_dtype, int32_t fp8_scale_format,
+                              ep_size_hint* out) {
+    ep_status st = ep::check_shape(sh);
+    if (st != EP_OK) return st;
+    if (out == nullptr) return EP_ERR_INVALID_ARG;
+    if (recv_dtype != EP_BF16 && recv_dtype != EP_FP8_E4M3) return EP_ERR_INVALID_ARG;
+    if (fp8_scale_format < EP_FP8_SCALE_FP32 || fp8_scale_format > EP_FP8_SCALE_TENSOR)
+        return EP_ERR_INVALID_ARG;
+    const uint64_t R = (uint64_t)sh->num_ranks, T = (uint64_t)sh->num_tokens,
+                   H = (uint64_t)sh->hidden, k = (uint64_t)sh->num_topk,
+                   E = (uint64_t)sh->num_experts, E_loc = E / R,
+                   nmax = (uint64_t)sh->num_max_dispatch_tokens_per_rank, G = H / EP_FP8_GROUP;
+    const bool fp8 = recv_dtype == EP_FP8_E4M3;
+    const uint64_t elem = fp8 ? 1 : 2;
+    const uint64_t scale = fp8 ? (fp8_scale_format == EP_FP8_SCALE_UE8M0 ? 1 : 4) : 0;
+    bool bad = false;
+    auto mul = [&bad](uint64_t a, uint64_t b) {
+        uint64_t r = 0;
+        if (__builtin_mul_overflow(a, b, &r)) bad = true;
+        return r;
+    };
+    ep_size_hint h{};
+    const uint64_t rows = mul(mul(R, R), T);
+    h.recv_rows = (int64_t)rows;
+    h.recv_x_bytes = mul(mul(rows, H), elem);
+    h.recv_x_scales_bytes = mul(mul(rows, G), scale);
+    h.recv_topk_idx_bytes = mul(mul(rows, k), 8);
+    h.recv_topk_weights_bytes = mul(mul(rows, k), 4);
+    h.recv_src_idx_bytes = mul(rows, 4);
+    const uint64_t em_rows = mul(rows, k < E_loc ? k : E_loc);
+    h.expert_major_rows = (int64_t)em_rows;
+    h.expert_major_x_bytes = mul(mul(em_rows, H), elem);
+    const uint64_t slots = mul(mul(mul(R, E_loc), R), nmax);
+    h.ll_slots = slots;
+    h.ll_recv_x_bytes = mul(mul(slots, H), elem);
+    h.ll_recv_x_scales_bytes = mul(mul(slots, G), scale);
+    h.ll_src_info_bytes = mul(slots, 4);
+    h.ll_slot_bytes = mul(mul(mul(R, T), k), 4);
+    h.ll_send_count_bytes = mul(mul(E, R), 4);
+    h.ll_recv_expert_count_bytes = mul(E, 4);
+    h.ll_layout_range_bytes = mul(mul(E, R), 8);
+    h.layout_workspace_bytes = ep_layout_workspace_size(sh);
+    if (bad || rows > (uint64_t)INT64_MAX || em_rows > (uint64_t)INT64_MAX) return EP_ERR_UNSUPPORTED;
+    *out = h;
+    return EP_OK;
+}
+
 const char* ep_status_string(ep_status status) {
     switch (status) {
         case EP_OK: return "EP_OK";
@@ -131,6 +178,6 @@ const char* ep_last_cuda_error(void) { return ep::g_last_error; }
 
 uint64_t ep_kernel_launch_count(void) { return ep::g_launches.load(std::memory_order_relaxed); }
 
-int32_t ep_abi_version(void) { return 101; }
+int32_t ep_abi_version(void) { return 102; }
 
 }  // extern "C"

@@ -405,6 +405,42 @@ EP_API ep_status ep_clean_ll_buffer(const ep_shape* shape, ep_ll_buffer* buf, co
 
 /* ---------------------------------------------------------------- helpers */
 
+/* Buffer sizes for one shape, in bytes unless named rows: the caller-owned counterpart of
+ * the pages' buffer size hints ([README] normal-kernel example: Buffer sizing with
+ * get_dispatch_config / get_combine_config and the NVL / RDMA size hints; low-latency
+ * example: get_low_latency_rdma_size_hint). Worst cases need no host synchronisation:
+ *   recv_rows          R*R*T: every token of every source reaching every destination
+ *                      (row_offset[d] = d*R*T); recv_* sizes are for that many rows
+ *   expert_major_rows  R*R*T*min(k, E_loc): one row per entry, at most min(k, E_loc)
+ *                      entries of a token per destination
+ *   ll_*               the low-latency buffer of ep_ll_buffer (R*E_loc*R*Nmax slots)
+ *   layout_workspace   ep_layout_workspace_size
+ * recv_dtype selects the row element (2 bytes bf16, 1 byte e4m3); scale sizes are 0 for
+ * bf16, 1 byte per group with EP_FP8_SCALE_UE8M0, else 4. Returns EP_ERR_UNSUPPORTED if a
+ * size does not fit in 64 bits. Host only; launches nothing. */
+typedef struct ep_size_hint {
+    int64_t recv_rows;
+    uint64_t recv_x_bytes;
+    uint64_t recv_x_scales_bytes;
+    uint64_t recv_topk_idx_bytes;
+    uint64_t recv_topk_weights_bytes;
+    uint64_t recv_src_idx_bytes;
+    int64_t expert_major_rows;
+    uint64_t expert_major_x_bytes;
+    uint64_t ll_slots;
+    uint64_t ll_recv_x_bytes;
+    uint64_t ll_recv_x_scales_bytes;
+    uint64_t ll_src_info_bytes;
+    uint64_t ll_slot_bytes;
+    uint64_t ll_send_count_bytes;
+    uint64_t ll_recv_expert_count_bytes;
+    uint64_t ll_layout_range_bytes;
+    uint64_t layout_workspace_bytes;
+} ep_size_hint;
+
+EP_API ep_status ep_buffer_size_hint(const ep_shape* shape, ep_dtype recv_dtype,
+                                     int32_t fp8_scale_format, ep_size_hint* out);
+
 /* The pages' implicit CPU wait for the received count ([README] note after
  * combine_backward): copies rank_prefix_matrix[R-1][*] (N_d per destination) into
  * host_counts[R] and synchronises `stream`. */

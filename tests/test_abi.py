@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(ep):
 
 
 def test_host_only_helpers(ep):
-    assert ep.ep_abi_version() == 101
+    assert ep.ep_abi_version() == 102
     assert ep.ep_kernel_launch_count() >= 0
     assert ep.lib().ep_status_string(1).startswith(b"EP_ERR_INVALID_ARG")
     assert ep.lib().ep_last_cuda_error() == b""
@@ -121,3 +121,41 @@ def test_invalid_arguments_rejected_on_host(ep):
     st = L.ep_dispatch(ctypes.byref(big), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,
                        ctypes.byref(h), ctypes.byref(out), ctypes.byref(launch))
     assert st == ep.EP_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("recv_dtype,fmt", [(0, 0), (1, 0), (1, 2)])
+def test_buffer_size_hint_matches_the_python_buffers(ep, recv_dtype, fmt):
+    """ep_buffer_size_hint (host only) against the sizes the binding's buffer classes
+    allocate for the same shape (CPU tensors; nothing runs on a GPU)."""
+    import torch
+    from combine_layout_02_gb300.buffers import LLBuffers, RecvBuffers, worst_case_row_offsets
+    sh = ep.make_shape(4, 37, 256, 16, 6, 5, nmax=40)
+    h = ep.ep_buffer_size_hint(sh, recv_dtype, fmt)
+    rows = worst_case_row_offsets(4, 37)[-1]
+    assert h["recv_rows"] == rows == 4 * 4 * 37
+    rb = RecvBuffers(rows, 256, 6, recv_dtype=recv_dtype, device="cpu", fp8_scale=fmt)
+    nbytes = lambda t: 0 if t is None else t.numel() * t.element_size()   # noqa: E731
+    assert h["recv_x_bytes"] == nbytes(rb.recv_x)
+    assert h["recv_x_scales_bytes"] == nbytes(rb.recv_x_scales)
+    assert h["recv_topk_idx_bytes"] == nbytes(rb.recv_topk_idx)
+    assert h["recv_topk_weights_bytes"] == nbytes(rb.recv_topk_weights)
+    assert h["recv_src_idx_bytes"] == nbytes(rb.recv_src_idx)
+    assert h["expert_major_rows"] == rows * min(6, 16 // 4)
+    ll = LLBuffers(sh, bool(recv_dtype), device="cpu", fp8_scale=fmt)
+    assert h["ll_slots"] == ll.src_info.numel()
+    for key in ("recv_x", "recv_x_scales", "src_info", "slot", "send_count", "recv_expert_count",
+                "layout_range"):
+        assert h[f"ll_{key}_bytes"] == nbytes(getattr(ll, key)), key
+    assert h["layout_workspace_bytes"] == ep.ep_layout_workspace_size(sh)
+    del torch
+
+
+def test_buffer_size_hint_rejects_bad_arguments_and_overflow(ep):
+    L = ep.lib()
+    h = ep.ep_size_hint()
+    sh = ep.make_shape(4, 37, 256, 16, 6, 5, nmax=40)
+    assert L.ep_buffer_size_hint(ctypes.byref(sh), 7, 0, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_buffer_size_hint(ctypes.byref(sh), 1, 9, ctypes.byref(h)) == ep.EP_ERR_INVALID_ARG
+    assert L.ep_buffer_size_hint(ctypes.byref(sh), 0, 0, None) == ep.EP_ERR_INVALID_ARG
+    huge = ep.make_shape(64, 1 << 24, 1 << 30, 64, 8, 1, nmax=1 << 24)
+    assert L.ep_buffer_size_hint(ctypes.byref(huge), 0, 0, ctypes.byref(h)) == ep.EP_ERR_UNSUPPORTED
