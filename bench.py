@@ -189,7 +189,8 @@ def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
     user would run consecutive steps -- input copies, kernels and output copies on three
     streams with double-buffered device inputs and outputs, so step i+1's input copy and
     step i-1's output copy overlap step i's kernels (the two copy directions are
-    independent). `value` is the pipelined figure."""
+    independent). `value` is the pipelined figure: the median of three timed regions of
+    `e2e_steps` steps each."""
     import torch
     w = plan["w"]
     R, T, H, E, k, C = w.R, w.T, w.H, w.E, w.k, w.C
@@ -281,18 +282,25 @@ def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
     for i in range(4):
         issue(i)
     torch.cuda.synchronize()
-    barrier(world)
-    p0 = torch.cuda.Event(enable_timing=True)
-    p1 = torch.cuda.Event(enable_timing=True)
-    p0.record(s_in[0])
-    for i in range(e2e_steps):
-        issue(i)
-    for bb in range(2):
-        for c in range(nc):
-            s_in[0].wait_event(ev_out[bb][c])
-    p1.record(s_in[0])
-    torch.cuda.synchronize()
-    pipe_ms = reduce_max(p0.elapsed_time(p1) / e2e_steps, world, dev)
+
+    def pipelined_region():
+        barrier(world)
+        p0 = torch.cuda.Event(enable_timing=True)
+        p1 = torch.cuda.Event(enable_timing=True)
+        p0.record(s_in[0])
+        for i in range(e2e_steps):
+            issue(i)
+        for bb in range(2):
+            for c in range(nc):
+                s_in[0].wait_event(ev_out[bb][c])
+        p1.record(s_in[0])
+        torch.cuda.synchronize()
+        return reduce_max(p0.elapsed_time(p1) / e2e_steps, world, dev)
+
+    # The host link is shared with the machine's other work, and the overlap of the two
+    # copy directions varies between runs: three regions, the median is reported.
+    pipe_runs = [pipelined_region() for _ in range(3)]
+    pipe_ms = statistics.median(pipe_runs)
 
     h2d = x_h.numel() * x_h.element_size() + topk_h.numel() * 8 + wts_h.numel() * 4
     d2h = out_h[0].numel() * out_h[0].element_size()
@@ -315,6 +323,7 @@ def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
             "d2h_bytes_per_step": d2h,
             "mode": f"pipelined: input copies and output copies ({nc} streams each) and "
                     "kernels on their own streams, double-buffered device inputs/outputs",
+            "pipelined_ms_per_step_runs": [round(v, 4) for v in pipe_runs],
             "serial_ms_per_step": round(serial_ms, 4),
             "serial_value": round(world * total_bytes / (serial_ms * 1e6), 1),
             "link": link}
