@@ -11,7 +11,8 @@ resident in HBM, inputs larger than L2), timed over K steps with CUDA events onl
 the region, so the kernels chain through programmatic dependent launch as in use.
 `dispatch_gbs`, `combine_gbs`, `layout_dispatch_us` and `roofline` come from a second
 timed pass of the same K steps with CUDA events on the launching stream around every
-phase. `e2e` is the same metric through the same C-ABI
+phase. `layout_dispatch_synced_us` is the exact-size variant: layout, a host wait for the
+received counts, then the dispatch into regions of exactly those sizes. `e2e` is the same metric through the same C-ABI
 calls with host buffers: pinned host -> device copy of x / topk_idx / topk_weights and
 a device -> host copy of the combined output inside every timed step.
 
@@ -425,6 +426,20 @@ def make_plan(args, ep, dev, stream, launch):
             ep.ep_combine(sh, y, off, handle, ep.EP_COMBINE_WEIGHTED, topk, wts, None, out, None,
                           launch)
 
+        def layout_dispatch_synced():
+            # The pages' exact-size path: layout, the CPU waits for the received counts,
+            # then the dispatch writes into regions of exactly those sizes.
+            layout()
+            counts = ep.ep_read_recv_counts_sync(sh, handle, stream)
+            exact = [0]
+            for n in counts:
+                exact.append(exact[-1] + int(n))
+            ep.ep_dispatch(sh, x, ep.EP_BF16, None, ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16, topk, wts,
+                           handle, rb.recv_x, rb.recv_x_scales, rb.recv_topk_idx,
+                           rb.recv_topk_weights, rb.recv_src_idx, exact, launch)
+
+        if not reuse:
+            plan["layout_dispatch_synced"] = layout_dispatch_synced
         dname = "dispatch_fp8" if fp8 else "dispatch"
         # The plan owns every buffer whose raw pointers the calls use.
         plan["keep"] = (lb, rb, y, out, xs)
@@ -504,6 +519,27 @@ def make_plan(args, ep, dev, stream, launch):
     else:
         raise ValueError(args.workload)
     return plan
+
+
+def run_synced(args, world, dev, stream, call, reps=50):
+    """µs per layout + host wait for the received counts + dispatch into exact regions,
+    between CUDA events on the launching stream (the GPU idles while the host reads the
+    counts; that gap is part of the figure)."""
+    import torch
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    times = []
+    for _ in range(min(reps, max(args.steps, 3))):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return round(reduce_max(statistics.mean(times), world, dev) * 1e3, 2)
 
 
 def run_graph(args, world, dev, launch, step, flush_buf, total_bytes):
@@ -643,6 +679,12 @@ def run_ours(args, rank, world):
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flags set: {int(err.item())}")
 
+    synced = None
+    if "layout_dispatch_synced" in plan:
+        synced = run_synced(args, world, dev, stream, plan["layout_dispatch_synced"])
+        if int(err.item()) != 0:
+            raise RuntimeError(f"device error flags set: {int(err.item())}")
+
     e2e = None
     if args.workload == "dsv3" and not args.no_e2e:
         e2e = run_e2e(world, dev, plan, ep, err, total_bytes, max(4, min(args.steps, 20)),
@@ -689,6 +731,7 @@ def run_ours(args, rank, world):
                           "traffic": traffic_from_profiles(PHASE_KERNEL[dom]),
                           "algorithmic_bytes_per_launch": nbytes[dom]}
     result["e2e"] = e2e
+    result["layout_dispatch_synced_us"] = synced
     result["graph"] = graph
     result["timing"] = ("value / ms_per_step: K steps with events only around the region (around "
                         "each step when L2 is flushed); *_us, *_gbs and roofline: a second pass of K "
