@@ -614,16 +614,17 @@ def run_ours(args, rank, world):
     nbytes, units = plan["nbytes"]()
     total_bytes = sum(nbytes.values())
 
-    def timed_region(sampler, per_phase):
+    def timed_region(sampler, per_phase, flush=True):
         """K steps between a barrier and a synchronisation on each side. per_phase=False
         (the headline pass): events only around the whole region (around each step when
         L2 is flushed between steps, so the flush stays outside), so consecutive kernels
         overlap through programmatic dependent launch as they do in use. per_phase=True
         (the breakdown pass): an event before and after every phase."""
         n = args.steps
+        fbuf = flush_buf if flush else None
         if per_phase:
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(n)]
-        elif flush_buf is not None:
+        elif fbuf is not None:
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
         else:
             evs = None
@@ -636,8 +637,8 @@ def run_ours(args, rank, world):
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
         for i in range(n):
-            if flush_buf is not None:
-                flush_buf.zero_()
+            if fbuf is not None:
+                fbuf.zero_()
             if per_phase:
                 step(evs[i])
             elif evs is not None:
@@ -669,6 +670,12 @@ def run_ours(args, rank, world):
     # Per-phase breakdown (and the roofline's per-kernel durations): a second timed pass of
     # the same K steps with an event around every phase.
     phase_ms, per, _, phase_clocks = timed_region(ClockSampler(gpu_id), per_phase=True)
+    warm = None
+    if flush_buf is not None:
+        # Small working sets may stay in L2 between steps in use: the same steps unflushed.
+        warm_ms, _, _, _ = timed_region(None, per_phase=False, flush=False)
+        warm_ms = reduce_max(warm_ms / args.steps, world, dev)
+        warm = {"ms_per_step": round(warm_ms, 4), "note": "no L2 flush between steps"}
 
     ms_step = reduce_max(total_ms / args.steps, world, dev)
     flags = int(err.item())
@@ -732,6 +739,9 @@ def run_ours(args, rank, world):
                           "algorithmic_bytes_per_launch": nbytes[dom]}
     result["e2e"] = e2e
     result["layout_dispatch_synced_us"] = synced
+    if warm is not None:
+        warm["value"] = round(world * total_bytes / (warm["ms_per_step"] * 1e6), 1)
+        result["warm"] = warm
     result["graph"] = graph
     result["timing"] = ("value / ms_per_step: K steps with events only around the region (around "
                         "each step when L2 is flushed); *_us, *_gbs and roofline: a second pass of K "
