@@ -1,7 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by
 element, on seeded inputs spanning several tiles and ragged tails: the tiny workload,
-ragged shapes, R not a multiple of 8, R > 32, R = 1, R = 64, k = 32, empty inputs,
-masked entries, skewed and group-limited routing.
+ragged shapes, R not a multiple of 8, R > 32, R = 1, R = 64, k = 32, every expert chosen,
+8192 experts, 16384-wide rows, empty inputs, masked entries, skewed and group-limited
+routing.
 
 Bit-exact: every layout / handle tensor, receive rows (bf16 and e4m3), FP8 scales,
 recv_topk_idx / recv_topk_weights / recv_src_idx, low-latency slots and counts, and
@@ -31,6 +32,9 @@ CASES = {
     "r33": W("r33", R=33, T=50, H=256, E=66, k=3, C=4, seed=107),
     "k32": W("k32", R=8, T=64, H=128, E=64, k=32, C=3, seed=108),
     "many_channels": W("mc", R=2, T=9, H=128, E=8, k=2, C=12, seed=109),
+    "e8192": W("e8k", R=16, T=50, H=128, E=8192, k=8, C=3, seed=115),       # most experts
+    "h16k": W("h16k", R=4, T=33, H=16384, E=16, k=4, C=2, seed=116),       # 32 KB rows
+    "k_all": W("kall", R=4, T=40, H=256, E=32, k=32, C=5, seed=117),       # every expert
 }
 
 
