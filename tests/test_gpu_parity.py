@@ -414,3 +414,4 @@ def test_run_twice_bit_identical(name):
     for a, b in zip(*lls):
         np.testing.assert_array_equal(a, b)
     assert run.flags() == 0 and run_ll.flags() == 0
+
