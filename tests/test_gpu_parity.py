@@ -415,3 +415,25 @@ def test_run_twice_bit_identical(name):
         np.testing.assert_array_equal(a, b)
     assert run.flags() == 0 and run_ll.flags() == 0
 
+
+
+def test_dispatch_16_byte_aligned_buffers():
+    """x and the receive rows need only 16-byte alignment: buffers that start 16 bytes past
+    a 32-byte boundary give the oracle's bytes too."""
+    w, inp, run, ref = _setup("ragged")
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    n_x = w.R * w.T * w.H
+    xbuf = torch.empty(n_x + 8, dtype=torch.bfloat16, device="cuda")
+    x16 = xbuf[8:].view(w.R, w.T, w.H)
+    x16.copy_(run.x)
+    assert x16.data_ptr() % 32 == 16
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, fill_x=0xA5A5)
+    from combine_layout_02_gb300.buffers import RecvBuffers
+    rb = RecvBuffers(off[-1] + 1, w.H, w.k, with_topk=False, fill=0xA5)
+    recv16 = rb.recv_x.view(-1)[8: 8 + off[-1] * w.H].view(off[-1], w.H)
+    assert recv16.data_ptr() % 32 == 16
+    ep.ep_dispatch(run.sh, x16, ep.EP_BF16, None, ep.EP_BF16, None, None, run.lb.handle(rb.recv_src_idx),
+                   recv16, None, None, None, rb.recv_src_idx, off, run.launch)
+    np.testing.assert_array_equal(host_bits(recv16), exp["recv_x"])
+    assert run.flags() == 0
