@@ -70,7 +70,7 @@ def measured_peaks():
 
 
 KERNEL_SOURCES = {
-    "dispatch_kernel<copy>": ("dispatch.cu", "rowops.cuh", "ep_internal.cuh"),
+    "dispatch_tma_kernel": ("dispatch.cu", "rowops.cuh", "ep_internal.cuh"),
     "combine_kernel": ("combine.cu", "rowops.cuh", "ep_internal.cuh"),
 }
 
@@ -330,7 +330,7 @@ def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
             "link": link}
 
 
-PHASE_KERNEL = {"dispatch": "dispatch_kernel<copy>", "dispatch_fp8": "dispatch_kernel<quant>",
+PHASE_KERNEL = {"dispatch": "dispatch_tma_kernel", "dispatch_fp8": "dispatch_kernel<quant>",
                 "dispatch_em": "dispatch_em_kernel<copy>", "combine_em": "combine_em_kernel",
                 "combine": "combine_kernel", "layout": "layout_count+layout_prefix",
                 "ll_send": "ll_send_kernel", "ll_recv": "ll_recv_kernel",

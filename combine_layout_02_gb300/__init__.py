@@ -20,6 +20,7 @@ from typing import Optional, Sequence
 __all__ = [
     "EP_OK", "EP_ERR_INVALID_ARG", "EP_ERR_CUDA", "EP_ERR_UNSUPPORTED",
     "EP_DEVERR_BAD_EXPERT", "EP_DEVERR_RECV_OVERFLOW", "EP_DEVERR_SLOT_OVERFLOW",
+    "EP_DEVERR_TIMEOUT",
     "EP_BF16", "EP_FP8_E4M3", "EP_COMBINE_SUM", "EP_COMBINE_WEIGHTED",
     "EP_PHASE_SEND", "EP_PHASE_RECV", "EP_PHASE_BOTH", "EP_MAX_RANKS",
     "EP_FP8_SCALE_FP32", "EP_FP8_SCALE_POW2", "EP_FP8_SCALE_UE8M0", "EP_FP8_SCALE_TENSOR",
@@ -35,7 +36,7 @@ __all__ = [
 ]
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA, EP_ERR_UNSUPPORTED = 0, 1, 2, 3
-EP_DEVERR_BAD_EXPERT, EP_DEVERR_RECV_OVERFLOW, EP_DEVERR_SLOT_OVERFLOW = 1, 2, 4
+EP_DEVERR_BAD_EXPERT, EP_DEVERR_RECV_OVERFLOW, EP_DEVERR_SLOT_OVERFLOW, EP_DEVERR_TIMEOUT = 1, 2, 4, 8
 EP_BF16, EP_FP8_E4M3 = 0, 1
 EP_COMBINE_SUM, EP_COMBINE_WEIGHTED = 0, 1
 EP_PHASE_SEND, EP_PHASE_RECV, EP_PHASE_BOTH = 1, 2, 3

@@ -44,6 +44,62 @@ struct DispatchArgs {
     uint32_t* err;
 };
 
+// Destination rows of token g in ascending rank order into s_row / s_dst (overflowing
+// rows flagged and dropped), then the per-row metadata: recv_src_idx, and recv_topk_idx /
+// recv_topk_weights when the routing is given. Returns the number of destinations.
+__device__ __forceinline__ int token_rows_and_meta(const DispatchArgs& a, int64_t g, int t, int lane,
+                                                   int64_t* s_row, int* s_dst) {
+    int nd = 0;
+    for (int d0 = 0; d0 < a.R; d0 += 32) {
+        const int d = d0 + lane;
+        int64_t row = -1;
+        if (d < a.R) {
+            const int h = a.send_head[g * a.R + d];
+            if (h >= 0) {
+                row = a.off.v[d] + h;
+                if (row >= a.off.v[d + 1]) {
+                    raise_flag(a.err, EP_DEVERR_RECV_OVERFLOW);
+                    row = -1;
+                }
+            }
+        }
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
+        if (row >= 0) {
+            const int p = nd + __popc(bal & lanemask_lt());
+            s_row[p] = row;
+            s_dst[p] = d;
+        }
+        nd += __popc(bal);
+    }
+    __syncwarp();
+
+    if (a.recv_src_idx != nullptr)
+        for (int p = lane; p < nd; p += 32) a.recv_src_idx[s_row[p]] = t;
+    if (a.topk_idx != nullptr && lane < a.k) {
+        const int64_t e = a.topk_idx[g * a.k + lane];
+        const float wgt = a.topk_weights != nullptr ? a.topk_weights[g * a.k + lane] : 0.0f;
+        for (int p = 0; p < nd; ++p) {
+            const int64_t row = s_row[p];
+            const int d = s_dst[p];
+            const bool local = e >= 0 && e / a.E_loc == d;
+            a.recv_topk_idx[row * a.k + lane] = local ? e - (int64_t)d * a.E_loc : -1;
+            if (a.recv_topk_weights != nullptr)
+                a.recv_topk_weights[row * a.k + lane] = local ? wgt : 0.0f;
+        }
+    }
+    return nd;
+}
+
+// Pre-quantised input: the token's scales go to every destination row unchanged.
+__device__ __forceinline__ void copy_scale_rows(const DispatchArgs& a, int64_t g, const int64_t* s_row,
+                                                int nd, int lane) {
+    const int G = a.H >> 7;
+    const float* ss = a.x_scales + g * G;
+    float* rs = reinterpret_cast<float*>(a.recv_x_scales);
+    for (int p = 0; p < nd; ++p)
+        for (int i = lane; i < G; i += 32) rs[s_row[p] * G + i] = ss[i];
+}
+
 template <int MODE, int U>
 __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
@@ -51,7 +107,6 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kWarps;
     const int64_t out_row_bytes = (int64_t)a.H * (MODE == kQuant ? 1 : a.in_elem);
-    const int G = a.H >> 7;
     pdl_wait();
 
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
@@ -62,62 +117,73 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
         uint4 qa[U], qb[U];
         if (MODE == kQuant) quant_load<U>(src, a.H >> 4, 0, lane, 32, qa, qb);
 
-        // Destination rows in ascending rank order.
-        int nd = 0;
-        for (int d0 = 0; d0 < a.R; d0 += 32) {
-            const int d = d0 + lane;
-            int64_t row = -1;
-            if (d < a.R) {
-                const int h = a.send_head[g * a.R + d];
-                if (h >= 0) {
-                    row = a.off.v[d] + h;
-                    if (row >= a.off.v[d + 1]) {
-                        raise_flag(a.err, EP_DEVERR_RECV_OVERFLOW);
-                        row = -1;
-                    }
-                }
-            }
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
-            if (row >= 0) {
-                const int p = nd + __popc(bal & lanemask_lt());
-                s_row[warp][p] = row;
-                s_dst[warp][p] = d;
-            }
-            nd += __popc(bal);
-        }
-        __syncwarp();
-
-        // Per-row metadata.
-        if (a.recv_src_idx != nullptr)
-            for (int p = lane; p < nd; p += 32) a.recv_src_idx[s_row[warp][p]] = t;
-        if (a.topk_idx != nullptr && lane < a.k) {
-            const int64_t e = a.topk_idx[g * a.k + lane];
-            const float wgt = a.topk_weights != nullptr ? a.topk_weights[g * a.k + lane] : 0.0f;
-            for (int p = 0; p < nd; ++p) {
-                const int64_t row = s_row[warp][p];
-                const int d = s_dst[warp][p];
-                const bool local = e >= 0 && e / a.E_loc == d;
-                a.recv_topk_idx[row * a.k + lane] = local ? e - (int64_t)d * a.E_loc : -1;
-                if (a.recv_topk_weights != nullptr)
-                    a.recv_topk_weights[row * a.k + lane] = local ? wgt : 0.0f;
-            }
-        }
+        const int nd = token_rows_and_meta(a, g, t, lane, s_row[warp], s_dst[warp]);
 
         // Payload.
         if (MODE == kCopy) {
             scatter_copy_row<U>(src, a.recv_x, s_row[warp], nd, out_row_bytes, lane, 32);
-            if (a.copy_scales) {
-                const float* ss = a.x_scales + g * G;
-                float* rs = reinterpret_cast<float*>(a.recv_x_scales);
-                for (int p = 0; p < nd; ++p)
-                    for (int i = lane; i < G; i += 32) rs[s_row[warp][p] * G + i] = ss[i];
-            }
+            if (a.copy_scales) copy_scale_rows(a, g, s_row[warp], nd, lane);
         } else {
             scatter_quant_row_loaded<U>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
                                         s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
         }
         __syncwarp();
     }
+    pdl_trigger();
+}
+
+// Copy modes with bulk copies: one warp per source token. Lane 0 loads the token's row into
+// the warp's shared-memory buffer with one bulk copy (completion on an mbarrier) and, once
+// it has landed, stores it to every destination row with one bulk copy each; meanwhile the
+// warp's lanes compute the destination rows and write the metadata. The copy engine moves
+// the payload, so the SM issues a handful of instructions per row instead of one per 16
+// bytes, and a warp's next row can load while its previous stores drain. Waits are bounded:
+// a load that has not landed after kTmaMaxPolls polls (twice) raises EP_DEVERR_TIMEOUT and
+// the warp stores nothing more.
+constexpr int kTmaWarps = 4;
+constexpr int kTmaMaxPolls = 1 << 22;
+constexpr int kTmaSmemMax = 200 * 1024;    // shared-memory rows per block (4 rows <= 50 KB)
+
+__global__ void __launch_bounds__(kTmaWarps * 32) dispatch_tma_kernel(DispatchArgs a) {
+    extern __shared__ __align__(128) unsigned char rowbuf[];
+    __shared__ int64_t s_row[kTmaWarps][EP_MAX_RANKS];
+    __shared__ int s_dst[kTmaWarps][EP_MAX_RANKS];
+    __shared__ __align__(8) uint64_t s_bar[kTmaWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t row_bytes = (uint32_t)a.H * (uint32_t)a.in_elem;
+    unsigned char* buf = rowbuf + (size_t)warp * row_bytes;
+    const int64_t nw = (int64_t)gridDim.x * kTmaWarps;
+    if (lane == 0) mbar_init(&s_bar[warp], 1);
+    __syncwarp();
+    pdl_wait();
+
+    uint32_t parity = 0;
+    bool live = true;       // lane 0: false once a row load failed to land in time
+    for (int64_t g = (int64_t)blockIdx.x * kTmaWarps + warp; g < a.ntok; g += nw) {
+        const int t = (int)(g % a.T);
+        if (lane == 0 && live) {
+            bulk_wait_smem_read();                       // earlier stores have read buf
+            mbar_expect_bytes(&s_bar[warp], row_bytes);
+            bulk_load(buf, a.x + g * (int64_t)row_bytes, row_bytes, &s_bar[warp]);
+        }
+        const int nd = token_rows_and_meta(a, g, t, lane, s_row[warp], s_dst[warp]);
+        if (a.copy_scales) copy_scale_rows(a, g, s_row[warp], nd, lane);
+        if (lane == 0 && live) {
+            if (!mbar_wait_bounded(&s_bar[warp], parity, kTmaMaxPolls)) {
+                raise_flag(a.err, EP_DEVERR_TIMEOUT);
+                live = mbar_wait_bounded(&s_bar[warp], parity, kTmaMaxPolls);
+            }
+            if (live) {
+                parity ^= 1u;
+                fence_async_smem();
+                for (int p = 0; p < nd; ++p)
+                    bulk_store(a.recv_x + s_row[warp][p] * (int64_t)row_bytes, buf, row_bytes);
+                bulk_commit();
+            }
+        }
+        __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
     pdl_trigger();
 }
 
@@ -134,6 +200,32 @@ ep_status launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t strea
     }
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
     cudaError_t e = launch_pdl(dispatch_kernel<MODE, U>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
+    return e == cudaSuccess ? EP_OK : cuda_fail(e);
+}
+
+// Whether the copy fits the bulk-copy kernel: kTmaWarps rows of the token in shared memory.
+bool tma_copy_fits(const DispatchArgs& a) {
+    return (int64_t)kTmaWarps * a.H * a.in_elem <= kTmaSmemMax;
+}
+
+ep_status launch_dispatch_tma(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
+    if (a.ntok == 0) return EP_OK;
+    const size_t smem = (size_t)kTmaWarps * (size_t)a.H * (size_t)a.in_elem;
+    // Opt in to more than 48 KB of dynamic shared memory (per device, once is enough but
+    // the call is cheap and enqueues nothing).
+    cudaError_t e = cudaFuncSetAttribute(dispatch_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTmaSmemMax);
+    if (e != cudaSuccess) return cuda_fail(e);
+    int64_t blocks = (a.ntok + kTmaWarps - 1) / kTmaWarps;
+    if (num_sms > 0) {
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_tma_kernel, kTmaWarps * 32, smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const int64_t cap = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
+        if (blocks > cap) blocks = cap;
+    }
+    if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
+    e = launch_pdl(dispatch_tma_kernel, dim3((unsigned)blocks), dim3(kTmaWarps * 32), smem, stream, a);
     return e == cudaSuccess ? EP_OK : cuda_fail(e);
 }
 
@@ -207,6 +299,8 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)
         st = launch_dispatch<kQuant, 2>(a, sh->num_sms, launch->stream);
+    else if (tma_copy_fits(a))
+        st = launch_dispatch_tma(a, sh->num_sms, launch->stream);
     else
         st = launch_dispatch<kCopy, 8>(a, sh->num_sms, launch->stream);
     if (st != EP_OK) return st;

@@ -74,6 +74,7 @@ typedef int32_t ep_status;
 #define EP_DEVERR_BAD_EXPERT 1u    /* a topk_idx entry outside [-1, E) was skipped */
 #define EP_DEVERR_RECV_OVERFLOW 2u /* a row fell outside its receive region, skipped */
 #define EP_DEVERR_SLOT_OVERFLOW 4u /* a low-latency slot index reached Nmax, skipped */
+#define EP_DEVERR_TIMEOUT 8u       /* a bounded device wait gave up; the affected rows were skipped */
 
 typedef enum ep_dtype { EP_BF16 = 0, EP_FP8_E4M3 = 1 } ep_dtype;
 typedef enum ep_combine_mode { EP_COMBINE_SUM = 0, EP_COMBINE_WEIGHTED = 1 } ep_combine_mode;
