@@ -331,7 +331,7 @@ def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
 
 
 PHASE_KERNEL = {"dispatch": "dispatch_tma_kernel", "dispatch_fp8": "dispatch_kernel<quant>",
-                "dispatch_em": "dispatch_em_kernel<copy>", "combine_em": "combine_em_kernel",
+                "dispatch_em": "dispatch_em_tma_kernel", "combine_em": "combine_em_kernel",
                 "combine": "combine_kernel", "layout": "layout_count+layout_prefix",
                 "ll_send": "ll_send_kernel", "ll_recv": "ll_recv_kernel",
                 "ll_combine": "ll_combine_kernel"}

@@ -132,18 +132,11 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
     pdl_trigger();
 }
 
-// Copy modes with bulk copies: one warp per source token. Lane 0 loads the token's row into
-// the warp's shared-memory buffer with one bulk copy (completion on an mbarrier) and, once
-// it has landed, stores it to every destination row with one bulk copy each; meanwhile the
-// warp's lanes compute the destination rows and write the metadata. The copy engine moves
-// the payload, so the SM issues a handful of instructions per row instead of one per 16
-// bytes, and a warp's next row can load while its previous stores drain. Waits are bounded:
-// a load that has not landed after kTmaMaxPolls polls (twice) raises EP_DEVERR_TIMEOUT and
-// the warp stores nothing more.
-constexpr int kTmaWarps = 4;
-constexpr int kTmaMaxPolls = 1 << 22;
-constexpr int kTmaSmemMax = 200 * 1024;    // shared-memory rows per block (4 rows <= 50 KB)
-
+// Copy modes with bulk copies (tma_row_load / tma_row_store): one warp per source token;
+// while lane 0's row load is in flight the lanes compute the destination rows and write the
+// metadata. The copy engine moves the payload, so the SM issues a few instructions per row
+// instead of one per 16 bytes per destination, and a warp's next row can load while its
+// earlier stores drain.
 __global__ void __launch_bounds__(kTmaWarps * 32) dispatch_tma_kernel(DispatchArgs a) {
     extern __shared__ __align__(128) unsigned char rowbuf[];
     __shared__ int64_t s_row[kTmaWarps][EP_MAX_RANKS];
@@ -161,26 +154,11 @@ __global__ void __launch_bounds__(kTmaWarps * 32) dispatch_tma_kernel(DispatchAr
     bool live = true;       // lane 0: false once a row load failed to land in time
     for (int64_t g = (int64_t)blockIdx.x * kTmaWarps + warp; g < a.ntok; g += nw) {
         const int t = (int)(g % a.T);
-        if (lane == 0 && live) {
-            bulk_wait_smem_read();                       // earlier stores have read buf
-            mbar_expect_bytes(&s_bar[warp], row_bytes);
-            bulk_load(buf, a.x + g * (int64_t)row_bytes, row_bytes, &s_bar[warp]);
-        }
+        if (lane == 0 && live) tma_row_load(buf, a.x + g * (int64_t)row_bytes, row_bytes, &s_bar[warp]);
         const int nd = token_rows_and_meta(a, g, t, lane, s_row[warp], s_dst[warp]);
         if (a.copy_scales) copy_scale_rows(a, g, s_row[warp], nd, lane);
-        if (lane == 0 && live) {
-            if (!mbar_wait_bounded(&s_bar[warp], parity, kTmaMaxPolls)) {
-                raise_flag(a.err, EP_DEVERR_TIMEOUT);
-                live = mbar_wait_bounded(&s_bar[warp], parity, kTmaMaxPolls);
-            }
-            if (live) {
-                parity ^= 1u;
-                fence_async_smem();
-                for (int p = 0; p < nd; ++p)
-                    bulk_store(a.recv_x + s_row[warp][p] * (int64_t)row_bytes, buf, row_bytes);
-                bulk_commit();
-            }
-        }
+        if (lane == 0 && live)
+            live = tma_row_store(buf, a.recv_x, s_row[warp], nd, row_bytes, &s_bar[warp], parity, a.err);
         __syncwarp();
     }
     if (lane == 0) bulk_wait_all();

@@ -93,6 +93,40 @@ __global__ void __launch_bounds__(kThreads) dispatch_em_kernel(EmArgs a) {
     pdl_trigger();
 }
 
+// bf16 copy with bulk copies (tma_row_load / tma_row_store, as the rank-major dispatch):
+// one warp per source token, its valid entries' rows as destinations.
+__global__ void __launch_bounds__(kTmaWarps * 32) dispatch_em_tma_kernel(EmArgs a) {
+    extern __shared__ __align__(128) unsigned char rowbuf[];
+    __shared__ int64_t s_row[kTmaWarps][EP_MAX_TOPK];
+    __shared__ float s_coef[kTmaWarps][EP_MAX_TOPK];
+    __shared__ __align__(8) uint64_t s_bar[kTmaWarps];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t row_bytes = (uint32_t)a.H * 2u;
+    unsigned char* buf = rowbuf + (size_t)warp * row_bytes;
+    const int64_t nw = (int64_t)gridDim.x * kTmaWarps;
+    if (lane == 0) mbar_init(&s_bar[warp], 1);
+    __syncwarp();
+    pdl_wait();
+    uint32_t parity = 0;
+    bool live = true;       // lane 0: false once a row load failed to land in time
+    for (int64_t g = (int64_t)blockIdx.x * kTmaWarps + warp; g < a.ntok; g += nw) {
+        const int t = (int)(g % a.T);
+        if (lane == 0 && live) tma_row_load(buf, a.x + g * (int64_t)row_bytes, row_bytes, &s_bar[warp]);
+        const int nd = entry_rows(a, g, lane, s_row[warp], s_coef[warp]);
+        __syncwarp();
+        if (lane < nd) {
+            const int64_t row = s_row[warp][lane];
+            if (a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
+            if (a.recv_weights != nullptr) a.recv_weights[row] = s_coef[warp][lane];
+        }
+        if (lane == 0 && live)
+            live = tma_row_store(buf, a.recv_x, s_row[warp], nd, row_bytes, &s_bar[warp], parity, a.err);
+        __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+    pdl_trigger();
+}
+
 __global__ void __launch_bounds__(kThreads) combine_em_kernel(EmArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_TOPK];
     __shared__ float s_coef[kWarps][EP_MAX_TOPK];
@@ -170,10 +204,22 @@ ep_status ep_dispatch_expert_major(const ep_shape* sh, const void* x, ep_dtype r
     a.qm.tinv = fmt == EP_FP8_SCALE_TENSOR ? 1.0f / out->fp8.tensor_scale : 0.0f;
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (a.ntok > 0) {
-        const unsigned blocks = (unsigned)((a.ntok + kWarps - 1) / kWarps);
-        cudaError_t e = recv_dtype == EP_FP8_E4M3
-                            ? launch_pdl(dispatch_em_kernel<true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a)
-                            : launch_pdl(dispatch_em_kernel<false>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+        const size_t tma_smem = (size_t)kTmaWarps * (size_t)a.H * 2;
+        cudaError_t e = cudaSuccess;
+        if (recv_dtype == EP_FP8_E4M3) {
+            const unsigned blocks = (unsigned)((a.ntok + kWarps - 1) / kWarps);
+            e = launch_pdl(dispatch_em_kernel<true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+        } else if (tma_smem <= (size_t)kTmaSmemMax) {
+            e = cudaFuncSetAttribute(dispatch_em_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kTmaSmemMax);
+            const unsigned blocks = (unsigned)((a.ntok + kTmaWarps - 1) / kTmaWarps);
+            if (e == cudaSuccess)
+                e = launch_pdl(dispatch_em_tma_kernel, dim3(blocks), dim3(kTmaWarps * 32), tma_smem,
+                               launch->stream, a);
+        } else {
+            const unsigned blocks = (unsigned)((a.ntok + kWarps - 1) / kWarps);
+            e = launch_pdl(dispatch_em_kernel<false>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+        }
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);

@@ -42,6 +42,39 @@ __device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
     }
 }
 
+// Row moves with bulk copies (one warp per token, lane 0 issues everything): the row is
+// loaded into the warp's shared-memory buffer with one bulk copy and stored to each
+// destination row with one bulk copy. Blocks of kTmaWarps warps, one row buffer each.
+constexpr int kTmaWarps = 4;
+constexpr int kTmaMaxPolls = 1 << 22;      // bound on the polls of one mbarrier wait
+constexpr int kTmaSmemMax = 200 * 1024;    // dynamic shared memory a block may use
+
+// Lane 0: starts loading `bytes` from src into buf once the warp's earlier stores have
+// finished reading buf.
+__device__ __forceinline__ void tma_row_load(unsigned char* buf, const char* src, uint32_t bytes,
+                                             uint64_t* bar) {
+    bulk_wait_smem_read();
+    mbar_expect_bytes(bar, bytes);
+    bulk_load(buf, src, bytes, bar);
+}
+
+// Lane 0: waits (bounded, twice) for the row started by tma_row_load, then stores it to
+// rows[0..nd) of dst_base and commits the stores. A load that does not land raises
+// EP_DEVERR_TIMEOUT; returns false if it never landed (the caller then stops using buf).
+__device__ __forceinline__ bool tma_row_store(const unsigned char* buf, char* dst_base,
+                                              const int64_t* rows, int nd, uint32_t bytes,
+                                              uint64_t* bar, uint32_t& parity, uint32_t* err) {
+    if (!mbar_wait_bounded(bar, parity, kTmaMaxPolls)) {
+        raise_flag(err, EP_DEVERR_TIMEOUT);
+        if (!mbar_wait_bounded(bar, parity, kTmaMaxPolls)) return false;
+    }
+    parity ^= 1u;
+    fence_async_smem();
+    for (int p = 0; p < nd; ++p) bulk_store(dst_base + rows[p] * (int64_t)bytes, buf, bytes);
+    bulk_commit();
+    return true;
+}
+
 // FP8 e4m3 quantisation, one scale per 128 channels ("DeepEP" README feature notes:
 // FP8 dispatch with per-group scales; round_scale; use_ue8m0; fp8_quant_scale). Unit =
 // 16 channels (32 bytes of bf16 in, 16 bytes of e4m3 out); 8 consecutive units (8
