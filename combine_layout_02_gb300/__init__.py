@@ -31,8 +31,8 @@ __all__ = [
     "ep_buffer_size_hint", "ep_size_hint",
     "ep_dispatch", "ep_combine", "ep_dispatch_expert_major", "ep_combine_expert_major",
     "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
-    "ep_read_error_flags_sync", "ep_kernel_launch_count", "ep_abi_version",
-    "EXPORTED_SYMBOLS",
+    "ep_read_error_flags_sync", "ep_selftest_wait_timeout", "ep_kernel_launch_count",
+    "ep_abi_version", "EXPORTED_SYMBOLS",
 ]
 
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_CUDA, EP_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -52,8 +52,8 @@ EXPORTED_SYMBOLS = (
     "ep_buffer_size_hint",
     "ep_dispatch", "ep_combine", "ep_dispatch_expert_major", "ep_combine_expert_major",
     "ep_ll_dispatch", "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
-    "ep_read_error_flags_sync", "ep_status_string", "ep_last_cuda_error",
-    "ep_kernel_launch_count", "ep_abi_version",
+    "ep_read_error_flags_sync", "ep_selftest_wait_timeout", "ep_status_string",
+    "ep_last_cuda_error", "ep_kernel_launch_count", "ep_abi_version",
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -155,6 +155,7 @@ def lib():
         L.ep_clean_ll_buffer.argtypes = [S(ep_shape), S(ep_ll_buffer), S(ep_launch)]
         L.ep_read_recv_counts_sync.argtypes = [S(ep_shape), S(ep_handle), _P, _P]
         L.ep_read_error_flags_sync.argtypes = [_P, _P, _P]
+        L.ep_selftest_wait_timeout.argtypes = [_P, _I32, _P, S(ep_launch)]
         L.ep_status_string.argtypes = [_I32]
         L.ep_status_string.restype = ctypes.c_char_p
         L.ep_last_cuda_error.argtypes = []
@@ -166,7 +167,7 @@ def lib():
         for name in ("ep_get_layout", "ep_get_layout_static_scratch", "ep_dispatch", "ep_combine",
                      "ep_dispatch_expert_major", "ep_combine_expert_major", "ep_ll_dispatch",
                      "ep_ll_combine", "ep_clean_ll_buffer", "ep_read_recv_counts_sync",
-                     "ep_read_error_flags_sync"):
+                     "ep_read_error_flags_sync", "ep_selftest_wait_timeout"):
             getattr(L, name).restype = _I32
         _lib = L
     return _lib
@@ -340,6 +341,13 @@ def ep_read_recv_counts_sync(shape: ep_shape, handle: ep_handle, stream=None) ->
                                         ctypes.cast(host, ctypes.c_void_p), _stream_handle(stream))
     _check("ep_read_recv_counts_sync", st)
     return list(host)
+
+
+def ep_selftest_wait_timeout(src16, timeout_ms: int, elapsed_us=None,
+                             launch: Optional[ep_launch] = None) -> None:
+    _check("ep_selftest_wait_timeout",
+           lib().ep_selftest_wait_timeout(_ptr(src16), timeout_ms, _ptr(elapsed_us),
+                                          ctypes.byref(launch or make_launch())))
 
 
 def ep_read_error_flags_sync(error_flags, stream=None) -> int:

@@ -89,7 +89,44 @@ ep_status load_row_offsets(const int64_t* host, int R, RowOffsets* out) {
 
 }  // namespace ep
 
+namespace ep {
+namespace {
+
+// One thread arms a barrier for 32 bytes and bulk-copies only 16 into shared memory, so
+// the barrier phase never completes and the bounded wait has to give up.
+__global__ void wait_timeout_probe_kernel(const void* src16, uint64_t timeout_ns, uint32_t* err,
+                                          uint32_t* elapsed_us) {
+    __shared__ __align__(128) unsigned char buf[32];
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    pdl_wait();
+    mbar_init(&bar, 1);
+    mbar_expect_bytes(&bar, 32);
+    bulk_load(buf, src16, 16, &bar);
+    const uint64_t t0 = global_ns();
+    const bool done = mbar_wait_bounded(&bar, 0, timeout_ns);
+    const uint64_t t1 = global_ns();
+    if (!done) raise_flag(err, EP_DEVERR_TIMEOUT);
+    if (elapsed_us != nullptr) *elapsed_us = (uint32_t)((t1 - t0) / 1000u);
+}
+
+}  // namespace
+}  // namespace ep
+
 extern "C" {
+
+ep_status ep_selftest_wait_timeout(const void* src16, int32_t timeout_ms, uint32_t* elapsed_us,
+                                   const ep_launch* launch) {
+    using namespace ep;
+    if (launch == nullptr || launch->error_flags == nullptr || src16 == nullptr) return EP_ERR_INVALID_ARG;
+    if (((uintptr_t)src16 & 15) != 0 || timeout_ms < 1 || timeout_ms > 10000) return EP_ERR_INVALID_ARG;
+    ep_status st = begin_call(launch);
+    if (st != EP_OK) return st;
+    cudaError_t e = launch_pdl(wait_timeout_probe_kernel, dim3(1), dim3(32), 0, launch->stream, src16,
+                               (uint64_t)timeout_ms * 1000000ull, launch->error_flags, elapsed_us);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return end_call(launch);
+}
 
 ep_status ep_read_recv_counts_sync(const ep_shape* shape, const ep_handle* handle,
                                    int32_t* host_counts, cudaStream_t stream) {

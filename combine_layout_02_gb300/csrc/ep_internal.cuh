@@ -105,10 +105,17 @@ __device__ __forceinline__ void mbar_expect_bytes(uint64_t* bar, uint32_t bytes)
                  : "memory");
 }
 
-// Waits for the barrier phase with parity `parity`, giving up after `max_polls` polls
-// (each poll may itself suspend the thread for a while). Returns whether it completed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int max_polls) {
-    for (int i = 0; i < max_polls; ++i) {
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the barrier phase with parity `parity`, giving up once `timeout_ns` of the
+// GPU's global timer have passed. Returns whether the phase completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    const uint64_t t0 = global_ns();
+    for (;;) {
         uint32_t done;
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; "
@@ -117,8 +124,8 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             : "r"(smem_addr(bar)), "r"(parity)
             : "memory");
         if (done) return true;
+        if (global_ns() - t0 > timeout_ns) return false;
     }
-    return false;
 }
 
 // global -> shared, completing `bytes` on `bar`.

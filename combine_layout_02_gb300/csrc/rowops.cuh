@@ -46,7 +46,7 @@ __device__ __forceinline__ void scatter_copy_row(const char* __restrict__ src,
 // loaded into the warp's shared-memory buffer with one bulk copy and stored to each
 // destination row with one bulk copy. Blocks of kTmaWarps warps, one row buffer each.
 constexpr int kTmaWarps = 4;
-constexpr int kTmaMaxPolls = 1 << 22;      // bound on the polls of one mbarrier wait
+constexpr uint64_t kTmaWaitNs = 1000000000ull;   // bound on one mbarrier wait: 1 s
 constexpr int kTmaSmemMax = 200 * 1024;    // dynamic shared memory a block may use
 
 // Lane 0: starts loading `bytes` from src into buf once the warp's earlier stores have
@@ -58,15 +58,15 @@ __device__ __forceinline__ void tma_row_load(unsigned char* buf, const char* src
     bulk_load(buf, src, bytes, bar);
 }
 
-// Lane 0: waits (bounded, twice) for the row started by tma_row_load, then stores it to
+// Lane 0: waits (at most 1 s, twice) for the row started by tma_row_load, then stores it to
 // rows[0..nd) of dst_base and commits the stores. A load that does not land raises
 // EP_DEVERR_TIMEOUT; returns false if it never landed (the caller then stops using buf).
 __device__ __forceinline__ bool tma_row_store(const unsigned char* buf, char* dst_base,
                                               const int64_t* rows, int nd, uint32_t bytes,
                                               uint64_t* bar, uint32_t& parity, uint32_t* err) {
-    if (!mbar_wait_bounded(bar, parity, kTmaMaxPolls)) {
+    if (!mbar_wait_bounded(bar, parity, kTmaWaitNs)) {
         raise_flag(err, EP_DEVERR_TIMEOUT);
-        if (!mbar_wait_bounded(bar, parity, kTmaMaxPolls)) return false;
+        if (!mbar_wait_bounded(bar, parity, kTmaWaitNs)) return false;
     }
     parity ^= 1u;
     fence_async_smem();

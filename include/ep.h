@@ -452,6 +452,17 @@ EP_API ep_status ep_read_recv_counts_sync(const ep_shape* shape, const ep_handle
 EP_API ep_status ep_read_error_flags_sync(const uint32_t* error_flags, uint32_t* host_flags,
                                    cudaStream_t stream);
 
+/* Diagnostic of the bounded device waits (the pages have no counterpart; the bulk-copy
+ * dispatch kernels wait on shared-memory barriers for their row loads, at most 1 s per
+ * wait). Launches one thread that arms a barrier for 32 bytes but bulk-copies only 16 bytes
+ * from src16, so the phase never completes: its wait must give up after timeout_ms (1 to
+ * 10000) and OR EP_DEVERR_TIMEOUT into launch->error_flags (required), writing the time the
+ * wait took to *elapsed_us (device, nullable). Nothing faults or hangs, and the context stays
+ * usable.
+ *   src16  dev, 16-byte aligned, at least 16 readable bytes (only read) */
+EP_API ep_status ep_selftest_wait_timeout(const void* src16, int32_t timeout_ms, uint32_t* elapsed_us,
+                                          const ep_launch* launch);
+
 /* Static description of a status code. */
 EP_API const char* ep_status_string(ep_status status);
 
