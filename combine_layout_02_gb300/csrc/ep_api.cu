@@ -215,6 +215,6 @@ const char* ep_last_cuda_error(void) { return ep::g_last_error; }
 
 uint64_t ep_kernel_launch_count(void) { return ep::g_launches.load(std::memory_order_relaxed); }
 
-int32_t ep_abi_version(void) { return 102; }
+int32_t ep_abi_version(void) { return 103; }
 
 }  // extern "C"

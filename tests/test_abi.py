@@ -39,7 +39,7 @@ def test_every_declared_symbol_is_exported(ep):
 
 
 def test_host_only_helpers(ep):
-    assert ep.ep_abi_version() == 102
+    assert ep.ep_abi_version() == 103
     assert ep.ep_kernel_launch_count() >= 0
     assert ep.lib().ep_status_string(1).startswith(b"EP_ERR_INVALID_ARG")
     assert ep.lib().ep_last_cuda_error() == b""
