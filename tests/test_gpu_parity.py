@@ -437,3 +437,34 @@ def test_dispatch_16_byte_aligned_buffers():
                    recv16, None, None, None, rb.recv_src_idx, off, run.launch)
     np.testing.assert_array_equal(host_bits(recv16), exp["recv_x"])
     assert run.flags() == 0
+
+
+@pytest.mark.parametrize("num_sms", [1, 3])
+def test_num_sms_cap_persistent_grid(num_sms):
+    """ep_shape.num_sms caps the grid (Buffer.set_num_sms): each warp then walks many
+    tokens, reusing its row buffer and barrier phases. Results stay bit-exact."""
+    w, inp, run, ref = _setup("group8")
+    run.sh = ep.make_shape(w.R, w.T, w.H, w.E, w.k, w.C, num_sms=num_sms)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off)
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, inp["topk_idx"],
+                          inp["topk_weights"], fill_x=0xA5A5, fill_idx=-99, fill_w=-5.0, fill_src=-3)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb.recv_topk_idx), exp["recv_topk_idx"])
+    np.testing.assert_array_equal(host_bits(rb.recv_src_idx), exp["recv_src_idx"])
+    rq = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, with_topk=False)
+    eq = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, x_kind=oracle.X_QUANTIZE)
+    np.testing.assert_array_equal(host_bits(rq.recv_x), eq["recv_x"])
+    np.testing.assert_array_equal(host_bits(rq.recv_x_scales).view(np.uint32),
+                                  eq["recv_x_scales"].view(np.uint32))
+    q, sc = oracle.quantize_rows(inp["x"])
+    rp = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, with_topk=False,
+                      x=torch.from_numpy(q).cuda(), x_dtype=ep.EP_FP8_E4M3,
+                      x_scales=torch.from_numpy(sc).cuda())
+    np.testing.assert_array_equal(host_bits(rp.recv_x), eq["recv_x"])
+    out, _ = run.combine(rb.recv_x, off, ep.EP_COMBINE_WEIGHTED)
+    ec = oracle.combine(exp["recv_x"], ref["send_head"], np.array(off), w.E, w.k,
+                        ep.EP_COMBINE_WEIGHTED, inp["topk_idx"], inp["topk_weights"])
+    assert_close_bf16(host_bits(out), ec["out"])
+    assert run.flags() == 0
