@@ -311,6 +311,10 @@ EP_API ep_status ep_get_layout_static_scratch(const ep_shape* shape, const int64
  *                routing is undefined behaviour: the contract in [REUSE]
  *                "Performance Contract and Constraints"; it is not detected).
  *   out          receive buffers (see ep_recv); out->recv_src_idx may be the handle's.
+ * Copies (bf16, or pre-quantised e4m3) move each row with bulk copies (one load into shared
+ * memory, one store per destination) when 4 rows fit in 200 KB of shared memory, i.e.
+ * H * element size <= 50 KB; wider rows use 16-byte vector copies. A row load that has not
+ * landed after 1 s (twice) sets EP_DEVERR_TIMEOUT and the rows of that warp are skipped.
  * Overflowing rows: EP_DEVERR_RECV_OVERFLOW. */
 EP_API ep_status ep_dispatch(const ep_shape* shape, const void* x, ep_dtype x_dtype,
                       const float* x_scales, ep_dtype recv_dtype, const int64_t* topk_idx,
@@ -355,7 +359,8 @@ EP_API ep_status ep_combine(const ep_shape* shape, const void* y, const int64_t*
  *                 index of each row), recv_topk_weights [rows] (nullable: the entry's
  *                 weight, one per row), row_offset (host [R+1]); recv_topk_idx must be
  *                 NULL (each row is one entry).
- * Overflowing rows: EP_DEVERR_RECV_OVERFLOW. */
+ * bf16 rows up to 50 KB move with bulk copies as in ep_dispatch (EP_DEVERR_TIMEOUT if a row
+ * load does not land in time). Overflowing rows: EP_DEVERR_RECV_OVERFLOW. */
 EP_API ep_status ep_dispatch_expert_major(const ep_shape* shape, const void* x, ep_dtype recv_dtype,
                                           const int64_t* topk_idx, const float* topk_weights,
                                           const ep_handle* handle, ep_recv* out,
