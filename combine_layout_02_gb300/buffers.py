@@ -22,6 +22,40 @@ def new_event(stream=None) -> torch.cuda.Event:
     return ev
 
 
+class EventOverlap:
+    """The pages' event handle for overlap ("How DeepEP Achieves Communication-Computation
+    Overlapping with EventOverlap", sections "CUDA Event Capture in Buffer" and "Explicit
+    Stream Waiting"): a CUDA event plus tensors to keep alive until the work before it is
+    done. Pass `.event` as a call's wait_event (previous_event) or record_event
+    (async_finish) through make_launch; current_stream_wait() makes the current stream wait
+    for it, and a `with` block waits on exit. Python sugar only: the C ABI takes the event."""
+
+    def __init__(self, event: Optional[torch.cuda.Event] = None, extra_tensors: Sequence = ()):
+        self.event = event
+        self.extra_tensors = tuple(extra_tensors)
+
+    def current_stream_wait(self) -> None:
+        if self.event is not None:
+            torch.cuda.current_stream().wait_event(self.event)
+
+    def __enter__(self) -> "EventOverlap":
+        return self
+
+    def __exit__(self, *exc) -> None:
+        self.current_stream_wait()
+
+
+def capture(stream=None) -> EventOverlap:
+    """Buffer.capture(): an EventOverlap recorded now on `stream` (default: current)."""
+    return EventOverlap(new_event(stream))
+
+
+def completion_event(stream=None) -> EventOverlap:
+    """An EventOverlap to hand to a call as its record_event (async_finish): the call
+    records it after its last kernel."""
+    return EventOverlap(new_event(stream))
+
+
 class LayoutBuffers:
     """Outputs of ep_get_layout plus the handle tensors and the layout workspace."""
 

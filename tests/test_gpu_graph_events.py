@@ -211,3 +211,37 @@ def test_backward_identities_exact_on_integer_data():
     exp = oracle.combine(yd.view(torch.int16).cpu().numpy().view(np.uint16), ref["send_head"],
                          np.array(off), W.E, W.k, recv_topk_weights=gw)["combined_topk_weights"]
     np.testing.assert_allclose(cw.cpu().numpy(), exp, rtol=1e-5, atol=1e-6)
+
+
+def test_event_overlap_helpers_order_like_the_raw_events():
+    """capture() on the producer stream as previous_event, completion_event() as
+    async_finish, and EventOverlap.current_stream_wait / the `with` block on the consumer
+    side give the same ordering as raw events."""
+    from combine_layout_02_gb300.buffers import EventOverlap, capture, completion_event
+    inp = workloads.make_workload(W)
+    run = GpuRun(W.R, W.T, W.H, W.E, W.k, W.C, inp)
+    ref = oracle.layout(inp["topk_idx"], W.E, W.C)
+    run.layout()
+    torch.cuda.synchronize()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rng = np.random.default_rng(203)
+    x_new = workloads.make_hidden(rng, W.R, W.T, W.H)
+    x_new_d = dev_bf16(x_new)
+    x_buf = torch.zeros_like(run.x)
+    producer, comm = torch.cuda.Stream(), torch.cuda.Stream()
+    rb = RecvBuffers(off[-1], W.H, W.k, with_topk=False)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(producer):
+        torch.cuda._sleep(20_000_000)
+        x_buf.copy_(x_new_d)
+        previous = capture(producer)
+    finish = completion_event(comm)
+    launch = ep.make_launch(comm, wait_event=previous.event, record_event=finish.event)
+    ep.ep_dispatch(run.sh, x_buf, ep.EP_BF16, None, ep.EP_BF16, None, None,
+                   run.lb.handle(rb.recv_src_idx), rb.recv_x, None, None, None, rb.recv_src_idx,
+                   off, launch)
+    with EventOverlap(finish.event, extra_tensors=(rb.recv_x,)):
+        pass                                         # the current stream waits on exit
+    got = host_bits(rb.recv_x)
+    exp = oracle.dispatch(x_new, ref["send_head"], np.array(off), W.E)["recv_x"]
+    np.testing.assert_array_equal(got, exp)
