@@ -468,3 +468,33 @@ def test_num_sms_cap_persistent_grid(num_sms):
                         ep.EP_COMBINE_WEIGHTED, inp["topk_idx"], inp["topk_weights"])
     assert_close_bf16(host_bits(out), ec["out"])
     assert run.flags() == 0
+
+
+def test_rows_too_wide_for_bulk_copies_use_the_register_copy():
+    """bf16 rows above 50 KB (H > 25600) do not fit four shared-memory row buffers and take
+    the 16-byte register copy, rank-major and expert-major: still bit-exact."""
+    w = W("wide", R=2, T=21, H=26624, E=4, k=2, C=3, seed=118)
+    inp = workloads.make_workload(w)
+    run = GpuRun(w.R, w.T, w.H, w.E, w.k, w.C, inp)
+    ref = oracle.layout(inp["topk_idx"], w.E, w.C)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rb = run.dispatch(off)
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, inp["topk_idx"],
+                          inp["topk_weights"], fill_x=0xA5A5, fill_idx=-99, fill_w=-5.0, fill_src=-3)
+    np.testing.assert_array_equal(host_bits(rb.recv_x), exp["recv_x"])
+    np.testing.assert_array_equal(host_bits(rb.recv_topk_idx), exp["recv_topk_idx"])
+    from combine_layout_02_gb300.buffers import LayoutBuffers
+    lb = LayoutBuffers(run.sh, expert_major=True)
+    ep.ep_get_layout(run.sh, run.topk, lb.layout(), lb.handle(), lb.workspace, run.launch)
+    em = oracle.expert_layout(inp["topk_idx"], w.E)
+    eoff = [0]
+    for n in em["expert_prefix"][:, -1]:
+        eoff.append(eoff[-1] + int(n))
+    rx = torch.full((eoff[-1], w.H), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    ep.ep_dispatch_expert_major(run.sh, run.x, ep.EP_BF16, run.topk, run.wts, lb.handle(), rx, None,
+                                None, None, eoff, run.launch)
+    ee = oracle.dispatch_expert_major(inp["x"], inp["topk_idx"], inp["topk_weights"],
+                                      em["expert_rows"], np.array(eoff), w.E, fill_x=0xFFFF)
+    np.testing.assert_array_equal(host_bits(rx), ee["recv_x"])
+    assert run.flags() == 0
