@@ -9,7 +9,7 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (EP_BF16, EP_FP8_E4M3, EP_FP8_SCALE_FP32, EP_FP8_SCALE_UE8M0, EP_LL_LAYOUT_PACKED,
+from . import (EP_BF16, EP_FP8_SCALE_FP32, EP_FP8_SCALE_UE8M0, EP_LL_LAYOUT_PACKED,
                EP_LL_LAYOUT_SLOTS, ep_fp8_options,
                ep_handle, ep_layout, ep_layout_workspace_size, ep_ll_buffer, ep_shape, _ptr)
 
