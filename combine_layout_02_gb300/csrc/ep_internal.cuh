@@ -31,6 +31,20 @@ __device__ __forceinline__ void st_v4(void* p, const uint4& v) {
                  : "memory");
 }
 
+struct u32x8 {
+    uint32_t r[8];
+};
+
+// 32-byte load (sm_100+ ld .v8.b32); the address must be 32-byte aligned.
+__device__ __forceinline__ u32x8 ld_stream_v8(const void* p) {
+    u32x8 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v.r[0]), "=r"(v.r[1]), "=r"(v.r[2]), "=r"(v.r[3]), "=r"(v.r[4]),
+                   "=r"(v.r[5]), "=r"(v.r[6]), "=r"(v.r[7])
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void st_stream_v4(void* p, const uint4& v) {
     // Streaming store (evict-first): the written rows are far larger than L2.
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),

@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kTmaWarps * 32) dispatch_em_tma_kernel(EmArgs 
     pdl_trigger();
 }
 
+template <bool V32>
 __global__ void __launch_bounds__(kThreads) combine_em_kernel(EmArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_TOPK];
     __shared__ float s_coef[kWarps][EP_MAX_TOPK];
@@ -136,7 +137,11 @@ __global__ void __launch_bounds__(kThreads) combine_em_kernel(EmArgs a) {
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
         const int nd = entry_rows(a, g, lane, s_row[warp], s_coef[warp]);
         __syncwarp();
-        gather_reduce_row<kGatherU, kGatherP>(a.y, s_row[warp], s_coef[warp], nd, a.H,
+        if (V32)
+            gather_reduce_row32<2, 4>(a.y, s_row[warp], s_coef[warp], nd, a.H,
+                                      a.out + g * (int64_t)a.H * 2, lane, 32);
+        else
+            gather_reduce_row<kGatherU, kGatherP>(a.y, s_row[warp], s_coef[warp], nd, a.H,
                                               a.out + g * (int64_t)a.H * 2, lane, 32);
         __syncwarp();
     }
@@ -244,7 +249,10 @@ ep_status ep_combine_expert_major(const ep_shape* sh, const void* y, const int64
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (a.ntok > 0) {
         const unsigned blocks = (unsigned)((a.ntok + kWarps - 1) / kWarps);
-        cudaError_t e = launch_pdl(combine_em_kernel, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+        // 32-byte loads when y is 32-byte aligned (as the rank-major combine).
+        cudaError_t e = ((uintptr_t)y & 31) == 0
+                            ? launch_pdl(combine_em_kernel<true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a)
+                            : launch_pdl(combine_em_kernel<false>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);

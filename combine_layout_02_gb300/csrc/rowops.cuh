@@ -217,6 +217,64 @@ __device__ __forceinline__ void scatter_quant_row(const char* __restrict__ src,
     scatter_quant_row_loaded<U>(src, q_base, s_base, rows, nd, H, qm, first, stride, u_start, a, b);
 }
 
+// gather_reduce_row with 32-byte loads (16 channels per unit); y rows 32-byte aligned.
+template <int U, int P>
+__device__ __forceinline__ void gather_reduce_row32(const char* __restrict__ y_base,
+                                                    const int64_t* rows, const float* coef,
+                                                    int nd, int H, char* __restrict__ out_row,
+                                                    int first, int stride) {
+    const int units = H >> 4;
+    const int64_t row_bytes = (int64_t)H * 2;
+    for (int u0 = 0; u0 < units; u0 += stride * U) {
+        float acc[U][16];
+#pragma unroll
+        for (int i = 0; i < U; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[i][j] = 0.0f;
+        for (int p0 = 0; p0 < nd; p0 += P) {
+            u32x8 v[P][U];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (p0 + p < nd) {
+                    const char* src = y_base + rows[p0 + p] * row_bytes;
+#pragma unroll
+                    for (int i = 0; i < U; ++i) {
+                        const int u = u0 + i * stride + first;
+                        if (u < units) v[p][i] = ld_stream_v8(src + (int64_t)u * 32);
+                    }
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+                if (p0 + p < nd) {
+                    const float c = coef[p0 + p];
+#pragma unroll
+                    for (int i = 0; i < U; ++i)
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            acc[i][2 * j] = fmaf(c, bf16_lo(v[p][i].r[j]), acc[i][2 * j]);
+                            acc[i][2 * j + 1] = fmaf(c, bf16_hi(v[p][i].r[j]), acc[i][2 * j + 1]);
+                        }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < U; ++i) {
+            const int u = u0 + i * stride + first;
+            if (u < units) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 o = make_uint4(pack_bf16x2(acc[i][8 * h + 0], acc[i][8 * h + 1]),
+                                               pack_bf16x2(acc[i][8 * h + 2], acc[i][8 * h + 3]),
+                                               pack_bf16x2(acc[i][8 * h + 4], acc[i][8 * h + 5]),
+                                               pack_bf16x2(acc[i][8 * h + 6], acc[i][8 * h + 7]));
+                    st_v4(out_row + (int64_t)u * 32 + h * 16, o);
+                }
+            }
+        }
+    }
+}
+
 // out = sum_p coef[p] * rows[p], fp32 accumulation in registers, one bf16 RNE store.
 // Unit = 8 channels (16 bytes); units [u_begin, u_end) of the row. Rows are taken P at a
 // time with every load of the batch (P rows x U units) issued before the first

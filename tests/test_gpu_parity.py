@@ -498,3 +498,44 @@ def test_rows_too_wide_for_bulk_copies_use_the_register_copy():
                                       em["expert_rows"], np.array(eoff), w.E, fill_x=0xFFFF)
     np.testing.assert_array_equal(host_bits(rx), ee["recv_x"])
     assert run.flags() == 0
+
+
+def test_combine_16_byte_aligned_y_takes_the_16_byte_gather():
+    """y that is 16- but not 32-byte aligned uses the 16-byte-load gather (aligned y uses
+    32-byte loads): both match the oracle, rank-major and expert-major."""
+    w, inp, run, ref = _setup("zipf16")
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    rng = np.random.default_rng(w.seed + 4000)
+    y32 = rng.standard_normal((off[-1], w.H)).astype(np.float32)
+    yb = torch.from_numpy(y32).to(torch.bfloat16)
+    ybits = yb.view(torch.int16).numpy().view(np.uint16)
+    ybuf = torch.empty(off[-1] * w.H + 8, dtype=torch.bfloat16, device="cuda")
+    y16 = ybuf[8:].view(off[-1], w.H)
+    y16.copy_(yb.cuda())
+    assert y16.data_ptr() % 32 == 16
+    exp = oracle.combine(ybits, ref["send_head"], np.array(off), w.E, w.k, ep.EP_COMBINE_WEIGHTED,
+                         inp["topk_idx"], inp["topk_weights"])
+    for y in (yb.cuda(), y16):
+        out, _ = run.combine(y, off, ep.EP_COMBINE_WEIGHTED)
+        assert_close_bf16(host_bits(out), exp["out"])
+    from combine_layout_02_gb300.buffers import LayoutBuffers
+    lb = LayoutBuffers(run.sh, expert_major=True)
+    ep.ep_get_layout(run.sh, run.topk, lb.layout(), lb.handle(), lb.workspace, run.launch)
+    em = oracle.expert_layout(inp["topk_idx"], w.E)
+    eoff = [0]
+    for n in em["expert_prefix"][:, -1]:
+        eoff.append(eoff[-1] + int(n))
+    ye = rng.standard_normal((eoff[-1], w.H)).astype(np.float32)
+    yeb = torch.from_numpy(ye).to(torch.bfloat16)
+    ebuf = torch.empty(eoff[-1] * w.H + 8, dtype=torch.bfloat16, device="cuda")
+    ye16 = ebuf[8:].view(eoff[-1], w.H)
+    ye16.copy_(yeb.cuda())
+    eexp = oracle.combine_expert_major(yeb.view(torch.int16).numpy().view(np.uint16), inp["topk_idx"],
+                                       inp["topk_weights"], em["expert_rows"], np.array(eoff), w.E)
+    for y in (yeb.cuda(), ye16):
+        oute = torch.empty((w.R, w.T, w.H), dtype=torch.bfloat16, device="cuda")
+        ep.ep_combine_expert_major(run.sh, y, eoff, lb.handle(), ep.EP_COMBINE_WEIGHTED, run.topk,
+                                   run.wts, oute, run.launch)
+        assert_close_bf16(host_bits(oute), eexp)
+    assert run.flags() == 0
