@@ -100,7 +100,7 @@ __device__ __forceinline__ void copy_scale_rows(const DispatchArgs& a, int64_t g
         for (int i = lane; i < G; i += 32) rs[s_row[p] * G + i] = ss[i];
 }
 
-template <int MODE, int U>
+template <int MODE, int U, bool V32 = false>
 __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
     __shared__ int s_dst[kWarps][EP_MAX_RANKS];
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
         // Quantising: the row's first batch does not depend on the metadata, so its load
         // shares the metadata's memory round trip.
         uint4 qa[U], qb[U];
-        if (MODE == kQuant) quant_load<U>(src, a.H >> 4, 0, lane, 32, qa, qb);
+        if (MODE == kQuant) quant_load<U, V32>(src, a.H >> 4, 0, lane, 32, qa, qb);
 
         const int nd = token_rows_and_meta(a, g, t, lane, s_row[warp], s_dst[warp]);
 
@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
             scatter_copy_row<U>(src, a.recv_x, s_row[warp], nd, out_row_bytes, lane, 32);
             if (a.copy_scales) copy_scale_rows(a, g, s_row[warp], nd, lane);
         } else {
-            scatter_quant_row_loaded<U>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
-                                        s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
+            scatter_quant_row_loaded<U, V32>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
+                                             s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
         }
         __syncwarp();
     }
@@ -165,19 +165,19 @@ __global__ void __launch_bounds__(kTmaWarps * 32) dispatch_tma_kernel(DispatchAr
     pdl_trigger();
 }
 
-template <int MODE, int U>
+template <int MODE, int U, bool V32 = false>
 ep_status launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
     if (a.ntok == 0) return EP_OK;
     int64_t blocks = (a.ntok + kWarps - 1) / kWarps;
     if (num_sms > 0) {
         int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<MODE, U>, kThreads, 0);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<MODE, U, V32>, kThreads, 0);
         if (e != cudaSuccess) return cuda_fail(e);
         const int64_t cap = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    cudaError_t e = launch_pdl(dispatch_kernel<MODE, U>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
+    cudaError_t e = launch_pdl(dispatch_kernel<MODE, U, V32>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
     return e == cudaSuccess ? EP_OK : cuda_fail(e);
 }
 
@@ -275,7 +275,9 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;
-    if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)
+    if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3 && ((uintptr_t)x & 31) == 0)
+        st = launch_dispatch<kQuant, 2, true>(a, sh->num_sms, launch->stream);   // 32-byte loads
+    else if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)
         st = launch_dispatch<kQuant, 2>(a, sh->num_sms, launch->stream);
     else if (tma_copy_fits(a))
         st = launch_dispatch_tma(a, sh->num_sms, launch->stream);

@@ -158,13 +158,18 @@ __device__ __forceinline__ void store_quant_unit(uint8_t* __restrict__ q_base, v
 
 // Loads batch u0 of a row for quantisation: units u0 + i*stride + first (i < U), as two
 // 16-byte halves each; zero beyond the row (those lanes still take part in the shuffles).
-template <int U>
+// V32: one 32-byte load per unit (src 32-byte aligned) instead of two 16-byte loads.
+template <int U, bool V32 = false>
 __device__ __forceinline__ void quant_load(const char* __restrict__ src, int units, int u0, int first,
                                            int stride, uint4 (&a)[U], uint4 (&b)[U]) {
 #pragma unroll
     for (int i = 0; i < U; ++i) {
         const int u = u0 + i * stride + first;
-        if (u < units) {
+        if (u < units && V32) {
+            const u32x8 v = ld_stream_v8(src + (int64_t)u * 32);
+            a[i] = make_uint4(v.r[0], v.r[1], v.r[2], v.r[3]);
+            b[i] = make_uint4(v.r[4], v.r[5], v.r[6], v.r[7]);
+        } else if (u < units) {
             a[i] = ld_stream_v4(src + (int64_t)u * 32);
             b[i] = ld_stream_v4(src + (int64_t)u * 32 + 16);
         } else {
@@ -178,7 +183,7 @@ __device__ __forceinline__ void quant_load(const char* __restrict__ src, int uni
 // hold the batch at u_start, already loaded (the caller can issue that load before its
 // own metadata loads), and each next batch is loaded before the current one is
 // quantised and stored, so two batches per thread are in flight.
-template <int U>
+template <int U, bool V32 = false>
 __device__ __forceinline__ void scatter_quant_row_loaded(const char* __restrict__ src,
                                                          uint8_t* __restrict__ q_base,
                                                          void* __restrict__ s_base,
@@ -188,7 +193,7 @@ __device__ __forceinline__ void scatter_quant_row_loaded(const char* __restrict_
     const int units = H >> 4;
     for (int u0 = u_start; u0 < units; u0 += stride * U) {
         uint4 na[U], nb[U];
-        quant_load<U>(src, units, u0 + stride * U, first, stride, na, nb);
+        quant_load<U, V32>(src, units, u0 + stride * U, first, stride, na, nb);
 #pragma unroll
         for (int i = 0; i < U; ++i) {
             const int u = u0 + i * stride + first;

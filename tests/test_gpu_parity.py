@@ -429,13 +429,35 @@ def test_dispatch_16_byte_aligned_buffers():
     x16.copy_(run.x)
     assert x16.data_ptr() % 32 == 16
     exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, fill_x=0xA5A5)
-    from combine_layout_02_gb300.buffers import RecvBuffers
+    from combine_layout_02_gb300.buffers import LayoutBuffers, RecvBuffers
     rb = RecvBuffers(off[-1] + 1, w.H, w.k, with_topk=False, fill=0xA5)
     recv16 = rb.recv_x.view(-1)[8: 8 + off[-1] * w.H].view(off[-1], w.H)
     assert recv16.data_ptr() % 32 == 16
     ep.ep_dispatch(run.sh, x16, ep.EP_BF16, None, ep.EP_BF16, None, None, run.lb.handle(rb.recv_src_idx),
                    recv16, None, None, None, rb.recv_src_idx, off, run.launch)
     np.testing.assert_array_equal(host_bits(recv16), exp["recv_x"])
+    # fused e4m3 from a 16-byte-aligned x (two 16-byte loads per unit instead of one 32-byte)
+    eq = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, x_kind=oracle.X_QUANTIZE)
+    for x_in in (run.x, x16):
+        rq = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3, with_topk=False, x=x_in)
+        np.testing.assert_array_equal(host_bits(rq.recv_x), eq["recv_x"])
+        np.testing.assert_array_equal(host_bits(rq.recv_x_scales).view(np.uint32),
+                                      eq["recv_x_scales"].view(np.uint32))
+    lb = LayoutBuffers(run.sh, expert_major=True)
+    ep.ep_get_layout(run.sh, run.topk, lb.layout(), lb.handle(), lb.workspace, run.launch)
+    em = oracle.expert_layout(inp["topk_idx"], w.E)
+    eoff = [0]
+    for n in em["expert_prefix"][:, -1]:
+        eoff.append(eoff[-1] + int(n))
+    ee = oracle.dispatch_expert_major(inp["x"], inp["topk_idx"], inp["topk_weights"], em["expert_rows"],
+                                      np.array(eoff), w.E, quantize=True)
+    for x_in in (run.x, x16):
+        rx = torch.zeros((eoff[-1], w.H), dtype=torch.uint8, device="cuda")
+        rs = torch.zeros((eoff[-1], w.H // 128), dtype=torch.float32, device="cuda")
+        ep.ep_dispatch_expert_major(run.sh, x_in, ep.EP_FP8_E4M3, run.topk, run.wts, lb.handle(), rx, rs,
+                                    None, None, eoff, run.launch)
+        np.testing.assert_array_equal(host_bits(rx), ee["recv_x"])
+        np.testing.assert_array_equal(host_bits(rs).view(np.uint32), ee["recv_x_scales"].view(np.uint32))
     assert run.flags() == 0
 
 
