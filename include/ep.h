@@ -331,7 +331,8 @@ EP_API ep_status ep_dispatch(const ep_shape* shape, const void* x, ep_dtype x_dt
  *                        topk_weights over valid entries whose expert lives on d (the
  *                        weighted top-k reduce).
  * Accumulation is fp32 in registers, one bf16 round-to-nearest-even store.
- *   y            dev [rows][H] bf16, rows in the dispatch's row order
+ *   y            dev [rows][H] bf16, rows in the dispatch's row order; 16-byte aligned
+ *                (32-byte aligned y is read with 32-byte loads, otherwise 16-byte ones)
  *   y_row_offset HOST [R+1] int64, the same regions as the dispatch's row_offset
  *   topk_idx, topk_weights  dev [R][T][k]; required for WEIGHTED, else ignored
  *   recv_topk_weights       dev [rows][k] fp32, nullable: when given,
