@@ -20,12 +20,13 @@ from typing import Callable, List, Optional, Sequence, Tuple
 import torch
 
 from . import (EP_BF16, EP_COMBINE_SUM, EP_COMBINE_WEIGHTED, EP_FP8_E4M3, EP_FP8_SCALE_FP32,
-               EP_FP8_SCALE_UE8M0, EP_PHASE_BOTH, EP_PHASE_RECV, EP_PHASE_SEND, ep_combine, ep_dispatch,
-               ep_get_layout, ep_ll_combine, ep_ll_dispatch, ep_read_error_flags_sync,
-               ep_read_recv_counts_sync, make_launch, make_shape)
+               EP_FP8_SCALE_UE8M0, EP_PHASE_BOTH, EP_PHASE_RECV, EP_PHASE_SEND, ep_combine,
+               ep_combine_expert_major, ep_dispatch, ep_dispatch_expert_major, ep_get_layout,
+               ep_ll_combine, ep_ll_dispatch, ep_read_error_flags_sync, ep_read_recv_counts_sync,
+               make_launch, make_shape)
 from .buffers import EventOverlap, LayoutBuffers, LLBuffers, new_event, worst_case_row_offsets
 
-__all__ = ["Buffer", "DispatchHandle", "LowLatencyHandle"]
+__all__ = ["Buffer", "DispatchHandle", "ExpertMajorHandle", "LowLatencyHandle"]
 
 
 class DispatchHandle:
@@ -59,6 +60,17 @@ class DispatchHandle:
     @property
     def send_head(self) -> torch.Tensor:
         return self.layout.send_head
+
+
+class ExpertMajorHandle:
+    """Layout with the expert-major placement, and the region of every destination."""
+
+    def __init__(self, layout: LayoutBuffers, row_offset: List[int], expert_prefix: List[List[int]],
+                 num_tokens: int):
+        self.layout = layout
+        self.row_offset = row_offset
+        self.expert_prefix = expert_prefix
+        self.num_tokens = num_tokens
 
 
 class LowLatencyHandle:
@@ -239,6 +251,62 @@ class Buffer:
                                  "(the views dispatch returned); got separate tensors")
         n = row_offset[-1] - row_offset[0]
         return base.as_strided((max(n, 1),) + tuple(base.shape[1:]), base.stride())
+
+    # ----------------------------------------------------------------- expert-major
+    def dispatch_expert_major(self, x: torch.Tensor, topk_idx: torch.Tensor,
+                              topk_weights: Optional[torch.Tensor] = None, fp8: bool = False,
+                              fp8_scale: int = EP_FP8_SCALE_FP32, tensor_scale: float = 0.0):
+        """One row per valid (token, expert) entry, each destination's rows grouped by local
+        expert (contiguous blocks a grouped GEMM can take as they are; the README's
+        "specific format" for the received rows). The host reads the per-expert counts
+        (a CPU wait) to size exact regions. Returns (recv_x: R lists of E_loc row tensors,
+        or of (e4m3, scales) pairs; recv_src_idx and recv_weights: R lists of E_loc
+        tensors (the token index and the entry's weight of each row); handle)."""
+        R, T, H = x.shape[0], x.shape[1], x.shape[2]
+        E_loc = self.E // self.R
+        sh = self._shape(T)
+        lb = LayoutBuffers(sh, self.device, expert_major=True)
+        launch, _ = self._launch(None, False)
+        ep_get_layout(sh, topk_idx, lb.layout(), lb.handle(), lb.workspace, launch)
+        prefix = lb.expert_prefix.cpu().tolist()                 # the CPU wait
+        off = [0]
+        for d in range(R):
+            off.append(off[-1] + int(prefix[d][-1]))
+        rows = max(off[-1], 1)
+        if fp8:
+            rx = torch.empty((rows, H), dtype=torch.uint8, device=self.device)
+            sdt = torch.uint8 if fp8_scale == EP_FP8_SCALE_UE8M0 else torch.float32
+            rs = torch.empty((rows, H // 128), dtype=sdt, device=self.device)
+        else:
+            rx = torch.empty((rows, H), dtype=torch.bfloat16, device=self.device)
+            rs = None
+        ri = torch.empty((rows,), dtype=torch.int32, device=self.device)
+        rw = None if topk_weights is None else torch.empty((rows,), dtype=torch.float32, device=self.device)
+        ep_dispatch_expert_major(sh, x, EP_FP8_E4M3 if fp8 else EP_BF16, topk_idx, topk_weights,
+                                 lb.handle(), rx, rs, rw, ri, off, launch,
+                                 fp8_scale=fp8_scale if fp8 else EP_FP8_SCALE_FP32,
+                                 tensor_scale=tensor_scale if fp8 else 0.0)
+
+        def blocks(t):
+            if t is None:
+                return None
+            return [[t[off[d] + prefix[d][e]: off[d] + prefix[d][e + 1]] for e in range(E_loc)]
+                    for d in range(R)]
+        recv_x = [list(zip(a, b)) for a, b in zip(blocks(rx), blocks(rs))] if fp8 else blocks(rx)
+        return recv_x, blocks(ri), blocks(rw), ExpertMajorHandle(lb, off, prefix, T)
+
+    def combine_expert_major(self, y: torch.Tensor, handle: ExpertMajorHandle, topk_idx: torch.Tensor,
+                             topk_weights: Optional[torch.Tensor] = None):
+        """y: the grouped GEMM's output, one tensor of all rows in the dispatch's order.
+        Sums each token's entry rows, weighted by topk_weights when given. Returns
+        combined_x [R][T][H]."""
+        sh = self._shape(handle.num_tokens)
+        out = torch.empty((self.R, handle.num_tokens, self.H), dtype=torch.bfloat16, device=self.device)
+        launch, _ = self._launch(None, False)
+        mode = EP_COMBINE_WEIGHTED if topk_weights is not None else EP_COMBINE_SUM
+        ep_combine_expert_major(sh, y, handle.row_offset, handle.layout.handle(), mode, topk_idx,
+                                topk_weights, out, launch)
+        return out
 
     # ----------------------------------------------------------------- low latency
     def low_latency_dispatch(self, x: torch.Tensor, topk_idx: torch.Tensor,

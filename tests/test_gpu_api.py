@@ -1,7 +1,7 @@
 """The Buffer front end (combine_layout_02_gb300.api), shaped like the pages' Python API,
 against the oracle: layout, exact-region and worst-case dispatch, FP8 and pre-quantised
 dispatch, handle reuse, weighted combine and the weight reduction, and the low-latency
-calls with and without the receive hook."""
+calls with and without the receive hook, and the expert-major blocks."""
 import numpy as np
 import pytest
 import torch
@@ -131,3 +131,28 @@ def test_buffer_rejects_rows_in_separate_allocations():
     with pytest.raises(ValueError):
         buf.dispatch(x, handle=handle, topk_idx=topk)
     assert ep.EP_OK == 0
+
+
+def test_buffer_expert_major_blocks():
+    inp, x, topk, wts = _inputs()
+    buf = Buffer(W.R, W.E, W.H, W.k, W.C)
+    recv_x, recv_src, recv_w, handle = buf.dispatch_expert_major(x, topk, wts)
+    em = oracle.expert_layout(inp["topk_idx"], W.E)
+    off = handle.row_offset
+    exp = oracle.dispatch_expert_major(inp["x"], inp["topk_idx"], inp["topk_weights"], em["expert_rows"],
+                                       np.array(off), W.E)
+    E_loc = W.E // W.R
+    for d in range(W.R):
+        for e in range(E_loc):
+            a, b = off[d] + int(em["expert_prefix"][d][e]), off[d] + int(em["expert_prefix"][d][e + 1])
+            np.testing.assert_array_equal(host_bits(recv_x[d][e]), exp["recv_x"][a:b])
+            np.testing.assert_array_equal(host_bits(recv_src[d][e]), exp["recv_src_idx"][a:b])
+            np.testing.assert_array_equal(host_bits(recv_w[d][e]).view(np.uint32),
+                                          exp["recv_weights"][a:b].view(np.uint32))
+    y = recv_x[0][0]                                   # all rows start at the first block
+    rows = torch.as_strided(y, (off[-1], W.H), y.stride())
+    out = buf.combine_expert_major(rows, handle, topk, wts)
+    ref = oracle.combine_expert_major(exp["recv_x"], inp["topk_idx"], inp["topk_weights"],
+                                      em["expert_rows"], np.array(off), W.E, weighted=True)
+    assert_close_bf16(host_bits(out), ref)
+    assert buf.check_errors() == 0
