@@ -11,7 +11,8 @@
 // One warp per output token: the warp gathers the destination rows from send_head
 // (ascending rank order) and their coefficients (1, or the sum of the token's weights
 // whose experts live on that rank), then accumulates in fp32 registers and stores
-// bf16 once. Each received row is read exactly once.
+// bf16 once. Each received row is read exactly once, with 32-byte loads when y is
+// 32-byte aligned (16-byte loads otherwise).
 #include "rowops.cuh"
 
 namespace ep {

@@ -12,8 +12,14 @@
 //
 // One warp per source token: the warp reads the token's send_head row, compacts the
 // destination rows into shared memory (ballot + popc, ascending rank order), writes
-// the per-row metadata, then streams the payload. In one device memory the
-// all-to-all reduces to this scatter; nothing is exchanged between GPUs.
+// the per-row metadata, then moves the payload. In one device memory the all-to-all
+// reduces to this scatter; nothing is exchanged between GPUs. Three kernels:
+//   dispatch_tma_kernel      copies (bf16, or pre-quantised e4m3): one bulk copy loads
+//                            the row into shared memory, one bulk copy per destination
+//                            stores it (rows up to 50 KB);
+//   dispatch_kernel<copy>    the same copy with 16-byte vector loads / stores (wider rows);
+//   dispatch_kernel<quant>   fused e4m3 quantisation, software-pipelined row loads
+//                            (32-byte loads when x is 32-byte aligned).
 #include "rowops.cuh"
 
 namespace ep {
