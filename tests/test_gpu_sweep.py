@@ -24,7 +24,9 @@ pytestmark = pytest.mark.gpu
 LL_MAX_ELEMS = 1 << 25          # slot-buffer elements (R * E * Nmax * H) the sweep allows
 
 
-def _draw_cases(n=24, seed=2024):
+def _draw_cases(n=24, seed=2024, name="sweep", wide=False):
+    """wide=True also draws rows too wide for the bulk-copy buffers (H = 26624, on small
+    R*T) and a capped grid (num_sms), so warps walk many tokens."""
     rng = np.random.default_rng(seed)
     cases = []
     for i in range(n):
@@ -33,27 +35,34 @@ def _draw_cases(n=24, seed=2024):
         E = R * E_loc
         k = int(rng.integers(1, min(E, 32) + 1))
         T = int(rng.choice([0, 1, 2, 17, 64, 129, 300]))
-        H = int(rng.choice([128, 256, 384, 1024]))
+        H = int(rng.choice([128, 256, 384, 1024] + ([2048, 26624] if wide else [])))
+        if H > 2048 and R * T > 512:
+            H = 2048
         C = int(rng.integers(1, 13))
         mask_p = float(rng.choice([0.0, 0.15]))
         routing = "zipf" if rng.random() < 0.3 else "uniform"
-        cases.append(workloads.Workload(f"sweep{i}", R=R, T=T, H=H, E=E, k=k, C=C, mask_p=mask_p,
-                                        routing=routing, zipf_s=1.1 if routing == "zipf" else 0.0,
-                                        nmax=max(T, 1) + int(rng.integers(0, 5)), seed=5000 + i))
+        sms = int(rng.choice([0, 1, 5])) if wide else 0
+        cases.append((workloads.Workload(f"{name}{i}", R=R, T=T, H=H, E=E, k=k, C=C, mask_p=mask_p,
+                                         routing=routing, zipf_s=1.1 if routing == "zipf" else 0.0,
+                                         nmax=max(T, 1) + int(rng.integers(0, 5)), seed=5000 + i
+                                         + (1000 if wide else 0)), sms))
     return cases
 
 
-CASES = _draw_cases()
+CASES = _draw_cases() + _draw_cases(16, seed=2025, name="wide", wide=True)
 
 
-def _ids(w):
-    return f"{w.name}-R{w.R}-T{w.T}-H{w.H}-E{w.E}-k{w.k}-C{w.C}"
+def _ids(case):
+    w, sms = case
+    return f"{w.name}-R{w.R}-T{w.T}-H{w.H}-E{w.E}-k{w.k}-C{w.C}" + (f"-sms{sms}" if sms else "")
 
 
-@pytest.mark.parametrize("w", CASES, ids=_ids)
-def test_sweep_all_entry_points(w):
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_sweep_all_entry_points(case):
+    w, sms = case
     inp = workloads.make_workload(w)
     run = GpuRun(w.R, w.T, w.H, w.E, w.k, w.C, inp, nmax=w.nmax)
+    run.sh = ep.make_shape(w.R, w.T, w.H, w.E, w.k, w.C, nmax=w.nmax, num_sms=sms)
     expert_major = w.E <= ep.EP_EXPERT_MAJOR_MAX_EXPERTS
     # ---- layout + handle (+ expert-major placement)
     run.lb = LayoutBuffers(run.sh, expert_major=expert_major)
