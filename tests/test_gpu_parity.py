@@ -561,3 +561,26 @@ def test_combine_16_byte_aligned_y_takes_the_16_byte_gather():
                                    run.wts, oute, run.launch)
         assert_close_bf16(host_bits(oute), eexp)
     assert run.flags() == 0
+
+
+def test_clean_ll_buffer_zeroes_the_signals_and_counts():
+    """clean_low_latency_buffer: the count signals, receive counts and layout ranges are
+    zero afterwards, and the next dispatch into the same buffer is exact again."""
+    w, inp, run = _ll_setup("masked")
+    buf = run.ll_dispatch(True)
+    assert int(buf.recv_expert_count.sum().item()) > 0
+    ep.ep_clean_ll_buffer(run.sh, buf.struct(), run.launch)
+    torch.cuda.synchronize()
+    for key in ("send_count", "recv_expert_count", "layout_range"):
+        assert int(torch.count_nonzero(getattr(buf, key)).item()) == 0, key
+    run.ll_dispatch(True, buf=buf)
+    exp = oracle.ll_dispatch(inp["x"], inp["topk_idx"], w.E, w.nmax, True)
+    for key in ("slot", "recv_expert_count", "layout_range"):
+        np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
+    # ep_read_recv_counts_sync returns each destination's received row count
+    ref = oracle.layout(inp["topk_idx"], w.E, 3)
+    run3 = GpuRun(w.R, w.T, w.H, w.E, w.k, 3, inp)
+    run3.layout()
+    counts = ep.ep_read_recv_counts_sync(run3.sh, run3.lb.handle())
+    np.testing.assert_array_equal(counts, ref["rank_prefix_matrix"][-1])
+    assert run.flags() == 0
