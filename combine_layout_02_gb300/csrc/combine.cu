@@ -41,6 +41,25 @@ struct CombineArgs {
     uint32_t* err;
 };
 
+// Metadata of token g held by the warp's lanes: lanes < k its expert id and weight,
+// lane d (and d + 32) its send_head entry for destination d.
+struct TokenMeta {
+    int64_t e;
+    float w;
+    int h0, h1;
+};
+
+__device__ __forceinline__ TokenMeta load_meta(const CombineArgs& a, int64_t g, int lane) {
+    TokenMeta m{-1, 0.0f, -1, -1};
+    if (a.weighted && lane < a.k) {
+        m.e = a.topk_idx[g * a.k + lane];
+        m.w = a.topk_weights[g * a.k + lane];
+    }
+    if (lane < a.R) m.h0 = a.send_head[g * a.R + lane];
+    if (lane + 32 < a.R) m.h1 = a.send_head[g * a.R + lane + 32];
+    return m;
+}
+
 template <int U, int P, bool V32>
 __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
@@ -53,19 +72,15 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
         // Every metadata load of the token is issued at once: lanes < k read the token's
         // expert ids and weights, lanes < R its send_head entries. The coefficient of
         // rank d is then a sum over warp shuffles (entries in ascending order).
-        int rank_j = -1;
-        float w_j = 0.0f;
-        if (a.weighted && lane < a.k) {
-            const int64_t e = a.topk_idx[g * a.k + lane];
-            w_j = a.topk_weights[g * a.k + lane];
-            rank_j = e >= 0 ? (int)(e / a.E_loc) : -1;
-        }
+        const TokenMeta cur = load_meta(a, g, lane);
+        const int rank_j = cur.e >= 0 ? (int)(cur.e / a.E_loc) : -1;
+        const float w_j = cur.w;
         int nd = 0;
         for (int d0 = 0; d0 < a.R; d0 += 32) {
             const int d = d0 + lane;
             int64_t row = -1;
             if (d < a.R) {
-                const int h = a.send_head[g * a.R + d];
+                const int h = d0 == 0 ? cur.h0 : cur.h1;
                 if (h >= 0) {
                     row = a.off.v[d] + h;
                     if (row >= a.off.v[d + 1]) {
