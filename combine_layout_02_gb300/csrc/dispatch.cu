@@ -55,12 +55,22 @@ struct DispatchArgs {
 // recv_topk_weights when the routing is given. Returns the number of destinations.
 __device__ __forceinline__ int token_rows_and_meta(const DispatchArgs& a, int64_t g, int t, int lane,
                                                    int64_t* s_row, int* s_dst) {
+    // Every metadata load of the token first (one memory round trip): send_head entries
+    // (lanes d and d + 32), and the expert ids and weights (lanes < k).
+    const int h0 = lane < a.R ? a.send_head[g * a.R + lane] : -1;
+    const int h1 = lane + 32 < a.R ? a.send_head[g * a.R + lane + 32] : -1;
+    int64_t e = -1;
+    float wgt = 0.0f;
+    if (a.topk_idx != nullptr && lane < a.k) {
+        e = a.topk_idx[g * a.k + lane];
+        if (a.topk_weights != nullptr) wgt = a.topk_weights[g * a.k + lane];
+    }
     int nd = 0;
     for (int d0 = 0; d0 < a.R; d0 += 32) {
         const int d = d0 + lane;
         int64_t row = -1;
         if (d < a.R) {
-            const int h = a.send_head[g * a.R + d];
+            const int h = d0 == 0 ? h0 : h1;
             if (h >= 0) {
                 row = a.off.v[d] + h;
                 if (row >= a.off.v[d + 1]) {
@@ -82,8 +92,6 @@ __device__ __forceinline__ int token_rows_and_meta(const DispatchArgs& a, int64_
     if (a.recv_src_idx != nullptr)
         for (int p = lane; p < nd; p += 32) a.recv_src_idx[s_row[p]] = t;
     if (a.topk_idx != nullptr && lane < a.k) {
-        const int64_t e = a.topk_idx[g * a.k + lane];
-        const float wgt = a.topk_weights != nullptr ? a.topk_weights[g * a.k + lane] : 0.0f;
         for (int p = 0; p < nd; ++p) {
             const int64_t row = s_row[p];
             const int d = s_dst[p];
