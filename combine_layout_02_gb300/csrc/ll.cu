@@ -197,37 +197,36 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     // Packed: the earlier sources' counts come from the count kernel.
     if (a.packed) pdl_wait();
 
-    if (threadIdx.x < a.k) {
+    // Warp 0 (k <= 32 lanes) places the entries and compacts the valid rows in entry
+    // order with a ballot.
+    if (threadIdx.x < 32) {
         const int j = threadIdx.x;
-        const int64_t e = s_e[j];
         int64_t row = -1;
-        int32_t pos = -1;
-        if (e >= a.E || e < -1) {
-            raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
-        } else if (e >= 0) {
-            if (s_cnt[j] >= a.nmax) {
-                raise_flag(a.err, EP_DEVERR_SLOT_OVERFLOW);
-            } else {
-                const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
-                int start = s * a.nmax;
-                if (a.packed) {
-                    start = 0;
-                    for (int src = 0; src < s; ++src) start += a.send_count[e * a.R + src];
+        if (j < a.k) {
+            const int64_t e = s_e[j];
+            int32_t pos = -1;
+            if (e >= a.E || e < -1) {
+                raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
+            } else if (e >= 0) {
+                if (s_cnt[j] >= a.nmax) {
+                    raise_flag(a.err, EP_DEVERR_SLOT_OVERFLOW);
+                } else {
+                    const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
+                    int start = s * a.nmax;
+                    if (a.packed) {
+                        start = 0;
+                        for (int src = 0; src < s; ++src) start += a.send_count[e * a.R + src];
+                    }
+                    pos = start + s_cnt[j];
+                    row = ((int64_t)d * a.E_loc + el) * slots + pos;
+                    a.src_info[row] = t;
                 }
-                pos = start + s_cnt[j];
-                row = ((int64_t)d * a.E_loc + el) * slots + pos;
-                a.src_info[row] = t;
             }
+            a.slot[tok * a.k + j] = pos;
         }
-        a.slot[tok * a.k + j] = pos;
-        s_rows[j] = row;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int n = 0;
-        for (int j = 0; j < a.k; ++j)
-            if (s_rows[j] >= 0) s_rows[n++] = s_rows[j];
-        s_nv = n;
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
+        if (row >= 0) s_rows[__popc(bal & lanemask_lt())] = row;
+        if (j == 0) s_nv = __popc(bal);
     }
     __syncthreads();
     const int nv = s_nv;
@@ -288,28 +287,26 @@ __global__ void __launch_bounds__(kThreads) ll_combine_kernel(LLArgs a) {
     const int64_t tok = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
     pdl_wait();
-    if (threadIdx.x < a.k) {
+    if (threadIdx.x < 32) {                     // warp 0: rows and weights, compacted
         const int j = threadIdx.x;
-        const int64_t e = a.topk_idx[tok * a.k + j];
-        const int32_t pos = a.slot[tok * a.k + j];
         int64_t row = -1;
-        if (e >= 0 && e < a.E && pos >= 0 && pos < slots) {
-            const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
-            row = ((int64_t)d * a.E_loc + el) * slots + pos;
-        }
-        s_rows[j] = row;
-        s_w[j] = a.topk_weights[tok * a.k + j];
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int n = 0;
-        for (int j = 0; j < a.k; ++j)
-            if (s_rows[j] >= 0) {
-                s_rows[n] = s_rows[j];
-                s_w[n] = s_w[j];
-                ++n;
+        float w = 0.0f;
+        if (j < a.k) {
+            const int64_t e = a.topk_idx[tok * a.k + j];
+            const int32_t pos = a.slot[tok * a.k + j];
+            w = a.topk_weights[tok * a.k + j];
+            if (e >= 0 && e < a.E && pos >= 0 && pos < slots) {
+                const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
+                row = ((int64_t)d * a.E_loc + el) * slots + pos;
             }
-        s_nv = n;
+        }
+        const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
+        if (row >= 0) {
+            const int p = __popc(bal & lanemask_lt());
+            s_rows[p] = row;
+            s_w[p] = w;
+        }
+        if (j == 0) s_nv = __popc(bal);
     }
     __syncthreads();
     const int units = a.H >> 3;
