@@ -15,7 +15,9 @@
 //   layout_prefix_kernel -- per block: the prefix entries of its (s, c) from the
 //       partial counts (warp reductions), the expert totals, and send_head for its
 //       tokens by a block-wide exclusive scan of the rank bits (ballot + popc within a
-//       warp, shared-memory scan across warps).
+//       warp, shared-memory scan across warps). With the expert-major placement the
+//       same launch has extra blocks that scan the expert columns (and give the expert
+//       totals), so the placement kernel follows it directly.
 // Rows of destination d are ordered by (source rank, token), so
 //   send_head[s][t][d] = recv_channel_prefix_matrix[d][s][c(t)]
 //                        + #{t' < t in the same channel with is_token_in_rank}.
@@ -46,6 +48,7 @@ struct LayoutArgs {
     int32_t* expert_prefix;               // [R][E_loc + 1]
     int32_t* ws_etot;                     // [E] expert totals (workspace)
     int ew;                               // bitmask words per expert (expert-major ranks)
+    int scan_rows;                        // grid rows of expert column-scan blocks (0: none)
     uint32_t* err;
 };
 
@@ -125,6 +128,54 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
     for (int e = threadIdx.x; e < a.E; e += kThreads) we[e] = hist[e];
 }
 
+// Expert-major placement, first step (blocks of the prefix launch with blockIdx.y >= R):
+// one warp per expert e scans its counts over (source, channel) pairs in lexicographic
+// order, in place in the workspace (exclusive prefix), and writes its total (ws_etot[e],
+// which is also num_recv_tokens_per_expert) and its per-source sums
+// (num_tokens_per_expert[s][e], accumulated per warp in shared memory). Up to four
+// 32-value chunks are loaded before any is scanned, so most columns cost one round trip.
+// These blocks are the only readers of the expert counts in this launch, which is why
+// the prefix blocks leave the expert totals to them.
+__device__ __forceinline__ void expert_column_scan(const LayoutArgs& a, int sb, int (*acc)[EP_MAX_RANKS]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = sb * kWarps + warp;
+    const int n = a.R * a.C;
+    if (e >= a.E) return;                         // warp-uniform; no block barrier follows
+    for (int sp = lane; sp < a.R; sp += 32) acc[warp][sp] = 0;
+    __syncwarp();
+    int carry = 0;
+    for (int i0 = 0; i0 < n; i0 += 128) {
+        int v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q * 32 + lane;
+            v[q] = i < n ? a.ws_expert[(int64_t)i * a.E + e] : 0;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int i = i0 + q * 32 + lane;
+            int incl = v[q];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (i < n) {
+                a.ws_expert[(int64_t)i * a.E + e] = carry + incl - v[q];
+                if (v[q] != 0) atomicAdd(&acc[warp][i / a.C], v[q]);
+            }
+            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        }
+    }
+    __syncwarp();
+    if (a.num_tokens_per_expert != nullptr)
+        for (int sp = lane; sp < a.R; sp += 32) a.num_tokens_per_expert[(int64_t)sp * a.E + e] = acc[warp][sp];
+    if (lane == 0) {
+        a.ws_etot[e] = carry;
+        a.num_recv_per_expert[e] = carry;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
     constexpr int kDPerWarp = EP_MAX_RANKS / kWarps;   // destinations per warp, at most
     __shared__ int s_base[EP_MAX_RANKS];
@@ -137,6 +188,11 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
     const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
     pdl_trigger();
     pdl_wait();
+    if (s >= R) {                                 // expert column-scan block
+        expert_column_scan(a, (s - R) * C + c, s_warp_tot);
+        return;
+    }
+    const bool totals = a.scan_rows == 0;         // else the scan blocks write them
 
     // ---- Loads. Everything the block reads first is loaded before any store or
     // barrier, so the loads share one memory round trip.
@@ -167,13 +223,13 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
     // (2) Per-source expert totals: one (source, expert) pair per thread of the grid.
     const int p2 = b * kThreads + threadIdx.x;
     int sum2 = 0;
-    if (a.num_tokens_per_expert != nullptr && p2 < R * E) {
+    if (totals && a.num_tokens_per_expert != nullptr && p2 < R * E) {
         const int sp = p2 / E, e = p2 - sp * E;
 #pragma unroll 4
         for (int cp = 0; cp < C; ++cp) sum2 += a.ws_expert[((int64_t)sp * C + cp) * E + e];
     }
     // (3) Per-expert receive totals: one expert per warp of the grid.
-    const int e3 = b * kWarps + warp;
+    const int e3 = totals ? b * kWarps + warp : E;
     int sum3 = 0;
     if (e3 < E) {
 #pragma unroll 4
@@ -197,7 +253,7 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
             }
         }
     }
-    if (a.num_tokens_per_expert != nullptr) {
+    if (totals && a.num_tokens_per_expert != nullptr) {
         if (p2 < R * E) a.num_tokens_per_expert[p2] = sum2;
         // Grids smaller than R*E threads take the remaining pairs in further passes.
         for (int p = p2 + nblocks * kThreads; p < R * E; p += nblocks * kThreads) {
@@ -253,42 +309,8 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
 }
 
 // ---- Expert-major placement (optional): rows of destination d grouped by local expert,
-// then source rank, then token. Runs after the two kernels above, which leave the
-// per-(source, channel) expert counts in the workspace.
-
-// One warp per expert e: exclusive scan of its counts over (source, channel) pairs in
-// lexicographic order, in place in the workspace, and its total (ws_etot[e]). Up to four
-// 32-value chunks are loaded before any is scanned, so most columns cost one round trip.
-__global__ void __launch_bounds__(kThreads) layout_expert_scan_kernel(LayoutArgs a) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int e = blockIdx.x * kWarps + warp;
-    const int n = a.R * a.C;
-    pdl_trigger();
-    pdl_wait();
-    if (e >= a.E) return;
-    int carry = 0;
-    for (int i0 = 0; i0 < n; i0 += 128) {
-        int v[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = i0 + q * 32 + lane;
-            v[q] = i < n ? a.ws_expert[(int64_t)i * a.E + e] : 0;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int i = i0 + q * 32 + lane;
-            int incl = v[q];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (i < n) a.ws_expert[(int64_t)i * a.E + e] = carry + incl - v[q];
-            carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-    }
-    if (lane == 0) a.ws_etot[e] = carry;
-}
+// then source rank, then token. The column-scan blocks of the prefix launch (above)
+// turn the per-(source, channel) expert counts into column prefixes; then:
 
 // One block per (channel c, source s). Each entry's row = the expert's prefix on its
 // destination + the count of that expert in earlier (source, channel) pairs + the count
@@ -450,15 +472,16 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     a.ew = expert ? (a.E >= 6144 ? 1 : (6144 / a.E > 16 ? 16 : 6144 / a.E)) : 1;
     a.err = launch->error_flags;
 
+    // Expert-major placement: enough extra grid rows of the prefix launch for one warp
+    // per expert.
+    a.scan_rows = expert ? ceil_div(ceil_div(a.E, kWarps), a.C) : 0;
+
     if ((st = begin_call(launch)) != EP_OK) return st;
     const dim3 grid(a.C, a.R);
     const size_t smem = sizeof(int) * (size_t)(a.E + a.R);
     cudaError_t e = launch_pdl(layout_count_kernel, grid, dim3(kThreads), smem, launch->stream, a);
     if (e == cudaSuccess)
-        e = launch_pdl(layout_prefix_kernel, grid, dim3(kThreads), 0, launch->stream, a);
-    if (e == cudaSuccess && expert)
-        e = launch_pdl(layout_expert_scan_kernel, dim3((unsigned)ceil_div(a.E, kWarps)), dim3(kThreads), 0,
-                       launch->stream, a);
+        e = launch_pdl(layout_prefix_kernel, dim3(a.C, a.R + a.scan_rows), dim3(kThreads), 0, launch->stream, a);
     if (e == cudaSuccess && expert)
         e = launch_pdl(layout_expert_rows_kernel, grid, dim3(kThreads),
                        sizeof(uint32_t) * (size_t)a.E * (1 + (size_t)(a.ew | 1)), launch->stream, a);
