@@ -16,6 +16,11 @@ received counts, then the dispatch into regions of exactly those sizes. `e2e` is
 calls with host buffers: pinned host -> device copy of x / topk_idx / topk_weights and
 a device -> host copy of the combined output inside every timed step.
 
+--workload picks another step (group_limited, zipf_reuse, ll_decode, ll_decode_packed,
+dsv3_expert_major, dsv3_backward; see WORKLOAD_TEXT); --fp8-scale picks the scale format of
+the e4m3 sends. The roofline's traffic comes from the committed ncu counters only when
+they were taken on the same workload and kernel sources.
+
 --impl reference times the CPU oracle (test infrastructure; single-threaded C) on a
 bounded token sample of the same workload and prints the same metric.
 
@@ -85,9 +90,9 @@ def source_digest(files):
     return h.hexdigest()
 
 
-def traffic_from_profiles(kernel: str):
+def traffic_from_profiles(kernel: str, workload: str = "dsv3"):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+    on the current kernel sources and on `workload` (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -97,6 +102,8 @@ def traffic_from_profiles(kernel: str):
     if not e or kernel not in KERNEL_SOURCES:
         return None
     if e.get("source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
+        return None
+    if e.get("workload", "dsv3") != workload:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -331,6 +338,7 @@ def run_e2e(world, dev, plan, ep, err, total_bytes, e2e_steps, copy_streams=1):
 
 
 PHASE_KERNEL = {"dispatch": "dispatch_tma_kernel", "dispatch_fp8": "dispatch_kernel<quant>",
+                "combine_backward": "dispatch_tma_kernel", "dispatch_backward": "combine_kernel",
                 "dispatch_em": "dispatch_em_tma_kernel", "combine_em": "combine_em_kernel",
                 "combine": "combine_kernel", "layout": "layout_count+layout_prefix",
                 "ll_send": "ll_send_kernel", "ll_recv": "ll_recv_kernel",
@@ -351,8 +359,13 @@ WORKLOAD_TEXT = {
                          "weighted combine; worst-case regions R*T*min(k, E_loc) rows per rank",
     "ll_decode_packed": "ll_decode with the packed receive layout (no gaps between the sources' "
                         "rows of an expert; send phase = per-source count kernel + send kernel)",
+    "dsv3_backward": "dsv3 shape; layout and forward dispatch once, then per step the backward "
+                     "pair with the cached handle: combine_backward = dispatch of a fresh output "
+                     "gradient, dispatch_backward = sum combine of the received gradient rows "
+                     "with the received weights' gradient reduced per token",
 }
-BASE_WORKLOAD = {"dsv3_expert_major": "dsv3", "ll_decode_packed": "ll_decode"}
+BASE_WORKLOAD = {"dsv3_expert_major": "dsv3", "ll_decode_packed": "ll_decode", "dsv3_backward": "dsv3"}
+FP8_SCALE = {"fp32": 0, "pow2": 1, "ue8m0": 2, "tensor": 3}
 
 
 def workload_config(name: str):
@@ -380,6 +393,15 @@ def make_plan(args, ep, dev, stream, launch):
     wts = torch.from_numpy(inp["topk_weights"]).to(dev)
     Tt = R * T
     plan = {"w": w, "inp": inp, "x": x, "topk": topk, "wts": wts, "flush": False}
+    fmt = FP8_SCALE[args.fp8_scale]
+    if fmt != FP8_SCALE["fp32"] and args.workload not in ("group_limited", "ll_decode", "ll_decode_packed"):
+        raise SystemExit(f"--fp8-scale applies to the e4m3 workloads, not {args.workload}")
+    tscale = 0.0
+    if fmt == FP8_SCALE["tensor"]:
+        # Per-tensor scale: one value for the whole input (its amax over the e4m3 maximum).
+        xf = (inp["x"].view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+        tscale = float(np.abs(xf).max()) / 448.0
+    sbytes = 1 if fmt == FP8_SCALE["ue8m0"] else 4
 
     if args.workload in ("dsv3", "group_limited", "zipf_reuse"):
         sh = ep.make_shape(R, T, H, E, k, C)
@@ -388,7 +410,7 @@ def make_plan(args, ep, dev, stream, launch):
         fp8 = args.workload == "group_limited"
         reuse = args.workload == "zipf_reuse"
         rb = RecvBuffers(off[-1], H, k, recv_dtype=ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16,
-                         with_topk=not reuse, device=dev)
+                         with_topk=not reuse, device=dev, fp8_scale=fmt)
         out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
         layout_s, handle = lb.layout(), lb.handle(rb.recv_src_idx)
 
@@ -420,7 +442,8 @@ def make_plan(args, ep, dev, stream, launch):
             else:
                 ep.ep_dispatch(sh, xi, ep.EP_BF16, None, ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16,
                                topk, wts, handle, rb.recv_x, rb.recv_x_scales, rb.recv_topk_idx,
-                               rb.recv_topk_weights, rb.recv_src_idx, off, launch)
+                               rb.recv_topk_weights, rb.recv_src_idx, off, launch,
+                               fp8_scale=fmt, tensor_scale=tscale)
 
         def combine():
             ep.ep_combine(sh, y, off, handle, ep.EP_COMBINE_WEIGHTED, topk, wts, None, out, None,
@@ -436,7 +459,8 @@ def make_plan(args, ep, dev, stream, launch):
                 exact.append(exact[-1] + int(n))
             ep.ep_dispatch(sh, x, ep.EP_BF16, None, ep.EP_FP8_E4M3 if fp8 else ep.EP_BF16, topk, wts,
                            handle, rb.recv_x, rb.recv_x_scales, rb.recv_topk_idx,
-                           rb.recv_topk_weights, rb.recv_src_idx, exact, launch)
+                           rb.recv_topk_weights, rb.recv_src_idx, exact, launch,
+                           fp8_scale=fmt, tensor_scale=tscale)
 
         if not reuse:
             plan["layout_dispatch_synced"] = layout_dispatch_synced
@@ -451,7 +475,7 @@ def make_plan(args, ep, dev, stream, launch):
             lay = Tt * k * 8 + Tt * R * (1 + 4)
             meta_in = Tt * R * 4 + (0 if reuse else Tt * k * 12)
             meta_out = N * 4 + (0 if reuse else N * k * 12)
-            payload = N * H * (1 if fp8 else 2) + (N * (H // 128) * 4 if fp8 else 0)
+            payload = N * H * (1 if fp8 else 2) + (N * (H // 128) * sbytes if fp8 else 0)
             b = {dname: Tt * H * 2 + payload + meta_in + meta_out,
                  "combine": N * H * 2 + Tt * H * 2 + Tt * R * 4 + Tt * k * 12}
             if not reuse:
@@ -459,6 +483,42 @@ def make_plan(args, ep, dev, stream, launch):
             return b, N
         plan["nbytes"] = nbytes
         plan["l2"] = "inputs larger than L2; no flush"
+    elif args.workload == "dsv3_backward":
+        # [README] normal-kernel example: the backward of combine is a dispatch with the
+        # handle, the backward of dispatch a combine that also reduces the received weights'
+        # gradient. Layout and one forward dispatch (for recv_topk_weights, the stand-in for
+        # their gradient) run once, outside the timed steps.
+        sh = ep.make_shape(R, T, H, E, k, C)
+        off = worst_case_row_offsets(R, T)
+        lb = LayoutBuffers(sh, dev)
+        rb = RecvBuffers(off[-1], H, k, device=dev)
+        layout_s, handle = lb.layout(), lb.handle(rb.recv_src_idx)
+        ep.ep_get_layout(sh, topk, layout_s, handle, lb.workspace, launch)
+        ep.ep_dispatch(sh, x, ep.EP_BF16, None, ep.EP_BF16, topk, wts, handle, rb.recv_x, None,
+                       rb.recv_topk_idx, rb.recv_topk_weights, rb.recv_src_idx, off, launch)
+        rng = np.random.default_rng(w.seed + 78)
+        grad_out = (torch.from_numpy(workloads.make_hidden(rng, R, T, H).view(np.int16))
+                    .to(dev).view(torch.bfloat16))
+        grad_recv = torch.empty((off[-1], H), dtype=torch.bfloat16, device=dev)
+        grad_x = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
+        grad_w = torch.empty((R, T, k), dtype=torch.float32, device=dev)
+        plan["keep"] = (lb, rb, grad_out, grad_recv, grad_x, grad_w)
+        plan["out"] = grad_x
+        plan["phases"] = [
+            ("combine_backward", lambda: ep.ep_dispatch(sh, grad_out, ep.EP_BF16, None, ep.EP_BF16, None,
+                                                        None, handle, grad_recv, None, None, None,
+                                                        rb.recv_src_idx, off, launch)),
+            ("dispatch_backward", lambda: ep.ep_combine(sh, grad_recv, off, handle, ep.EP_COMBINE_SUM,
+                                                        None, None, rb.recv_topk_weights, grad_x, grad_w,
+                                                        launch)),
+        ]
+        plan["l2"] = "inputs larger than L2; no flush"
+
+        def nbytes():
+            N = int(lb.rank_prefix_matrix[-1].sum().item())
+            return {"combine_backward": Tt * H * 2 + N * H * 2 + Tt * R * 4 + N * 4,
+                    "dispatch_backward": N * H * 2 + Tt * H * 2 + Tt * R * 4 + N * k * 4 + Tt * k * 4}, N
+        plan["nbytes"] = nbytes
     elif args.workload == "dsv3_expert_major":
         sh = ep.make_shape(R, T, H, E, k, C)
         lb = LayoutBuffers(sh, dev, expert_major=True)
@@ -492,7 +552,7 @@ def make_plan(args, ep, dev, stream, launch):
     elif args.workload in ("ll_decode", "ll_decode_packed"):
         sh = ep.make_shape(R, T, H, E, k, C, nmax=w.nmax)
         packed = args.workload == "ll_decode_packed"
-        buf = LLBuffers(sh, True, device=dev, packed=packed)
+        buf = LLBuffers(sh, True, device=dev, packed=packed, fp8_scale=fmt, tensor_scale=tscale)
         ybuf = LLBuffers(sh, False, device=dev, packed=packed)
         ep.ep_ll_dispatch(sh, x, topk, False, ep.EP_PHASE_BOTH, ybuf.struct(), launch)
         out = torch.empty((R, T, H), dtype=torch.bfloat16, device=dev)
@@ -512,7 +572,7 @@ def make_plan(args, ep, dev, stream, launch):
         def nbytes():
             M = int((inp["topk_idx"] >= 0).sum())
             G = H // 128
-            return {"ll_send": Tt * H * 2 + M * (H + G * 4) + Tt * k * (8 + 4) + M * 4 + E * R * 4,
+            return {"ll_send": Tt * H * 2 + M * (H + G * sbytes) + Tt * k * (8 + 4) + M * 4 + E * R * 4,
                     "ll_recv": E * R * 4 + E * R * 8 + E * 4,
                     "ll_combine": M * H * 2 + Tt * H * 2 + Tt * k * (8 + 4 + 4)}, M
         plan["nbytes"] = nbytes
@@ -722,6 +782,8 @@ def run_ours(args, rank, world):
                    "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)",
                    "l2": plan["l2"]},
     }
+    if args.workload in ("group_limited", "ll_decode", "ll_decode_packed"):
+        result["config"]["fp8_scale"] = args.fp8_scale
     for name in mean_ms:
         short = name.replace("_fp8", "")
         result[f"{short}_us"] = round(mean_ms[name] * 1e3, 2)
@@ -735,7 +797,7 @@ def run_ours(args, rank, world):
     result["roofline"] = {"bound": "hbm", "kernel": PHASE_KERNEL[dom], "achieved": round(gbs[dom], 1),
                           "peak": peak, "unit": "GB/s", "frac": round(gbs[dom] / peak, 4),
                           "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                          "traffic": traffic_from_profiles(PHASE_KERNEL[dom]),
+                          "traffic": traffic_from_profiles(PHASE_KERNEL[dom], args.workload),
                           "algorithmic_bytes_per_launch": nbytes[dom]}
     result["e2e"] = e2e
     result["layout_dispatch_synced_us"] = synced
@@ -826,6 +888,8 @@ def main():
                     help="streams per copy direction in the pipelined end-to-end measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="dsv3",
                     help="dsv3 is the benchmark line; the others are extra measurements")
+    ap.add_argument("--fp8-scale", choices=sorted(FP8_SCALE), default="fp32",
+                    help="scale format of the e4m3 sends (group_limited, ll_decode*)")
     ap.add_argument("--nmax", type=int, default=0,
                     help="low-latency slot capacity override (profiler captures only)")
     ap.add_argument("--tokens", type=int, default=0,
