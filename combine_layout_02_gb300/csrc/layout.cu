@@ -49,6 +49,9 @@ struct LayoutArgs {
     int32_t* ws_etot;                     // [E] expert totals (workspace)
     int ew;                               // bitmask words per expert (expert-major ranks)
     int scan_rows;                        // grid rows of expert column-scan blocks (0: none)
+    int el_shift;                         // log2(E_loc) when E_loc is a power of two, else -1
+    int vec_ids;                          // topk rows load as 16-byte pairs (k even, aligned)
+    int vec_head;                         // send_head rows store as 16-byte quads (R % 4 == 0)
     uint32_t* err;
 };
 
@@ -97,10 +100,24 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
         if (t < t1) {
             const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t) * a.k;
             for (int j0 = 0; j0 < a.k; j0 += 8) {
-                // Issue the token's loads together, then use them.
+                // Issue the token's loads together (as 16-byte pairs when k is even), then
+                // use them.
                 int64_t e[8];
+                if (a.vec_ids) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) e[i] = (j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+                    for (int i = 0; i < 8; i += 2) {
+                        if (j0 + i < a.k) {
+                            const longlong2 v = __ldg(reinterpret_cast<const longlong2*>(row + j0 + i));
+                            e[i] = v.x;
+                            e[i + 1] = v.y;
+                        } else {
+                            e[i] = e[i + 1] = -1;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) e[i] = (j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     if (e[i] == -1) continue;
@@ -109,7 +126,8 @@ __global__ void __launch_bounds__(kThreads) layout_count_kernel(LayoutArgs a) {
                         continue;
                     }
                     atomicAdd(&hist[(int)e[i]], 1);
-                    mask |= 1ull << ((int)e[i] / a.E_loc);
+                    const int d = a.el_shift >= 0 ? (int)e[i] >> a.el_shift : (int)e[i] / a.E_loc;
+                    mask |= 1ull << d;
                 }
             }
             const int64_t off = ((int64_t)s * a.T + t) * a.R;
@@ -299,10 +317,25 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
         __syncthreads();
         const uint32_t lt = lanemask_lt();
         int32_t* out = a.send_head + ((int64_t)s * a.T + t) * R;
-        for (int d = 0; d < R; ++d) {
-            const bool in = (mask >> d) & 1ull;
-            const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
-            if (t < t1) out[d] = in ? s_warp_off[warp][d] + __popc(bal & lt) : -1;
+        if (a.vec_head) {
+            // Four destinations per 16-byte store.
+            for (int d0 = 0; d0 < R; d0 += 4) {
+                int v[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int d = d0 + q;
+                    const bool in = (mask >> d) & 1ull;
+                    const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+                    v[q] = in ? s_warp_off[warp][d] + __popc(bal & lt) : -1;
+                }
+                if (t < t1) *reinterpret_cast<int4*>(out + d0) = make_int4(v[0], v[1], v[2], v[3]);
+            }
+        } else {
+            for (int d = 0; d < R; ++d) {
+                const bool in = (mask >> d) & 1ull;
+                const unsigned bal = __ballot_sync(0xFFFFFFFFu, in);
+                if (t < t1) out[d] = in ? s_warp_off[warp][d] + __popc(bal & lt) : -1;
+            }
         }
         __syncthreads();
     }
@@ -472,6 +505,9 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     a.ew = expert ? (a.E >= 6144 ? 1 : (6144 / a.E > 16 ? 16 : 6144 / a.E)) : 1;
     a.err = launch->error_flags;
 
+    a.el_shift = (a.E_loc & (a.E_loc - 1)) == 0 ? __builtin_ctz((unsigned)a.E_loc) : -1;
+    a.vec_ids = (a.k % 2 == 0 && ((uintptr_t)topk_idx & 15) == 0) ? 1 : 0;
+    a.vec_head = (a.R % 4 == 0 && ((uintptr_t)handle->send_head & 15) == 0) ? 1 : 0;
     // Expert-major placement: enough extra grid rows of the prefix launch for one warp
     // per expert.
     a.scan_rows = expert ? ceil_div(ceil_div(a.E, kWarps), a.C) : 0;
