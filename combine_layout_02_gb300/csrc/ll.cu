@@ -15,8 +15,10 @@
 // slots; source s owns [s*Nmax, (s+1)*Nmax) and fills them in the order of its
 // (token, k) entries: entry (t, j) of source s with expert e takes slot
 //   s*Nmax + #{(t', j') before (t, j) in source s with expert e}.
-// The send kernel computes that count by a block-wide scan of the source's earlier
-// entries (at most Nmax*k of them), so no block waits on another. Extra blocks write
+// The send kernel computes that count by a block-wide scan of the source's entries in
+// earlier tokens (at most Nmax*k of them; one shared-memory lookup each, in a table from
+// expert to the token's entry), plus the token's own earlier entries with the same
+// expert (a match-any vote), so no block waits on another. Extra blocks write
 // the per-(destination, expert, source) count signals; the receive kernel only
 // reads those signals.
 //
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     __shared__ int s_cnt[EP_MAX_TOPK];
     __shared__ int64_t s_rows[EP_MAX_TOPK];
     __shared__ int s_nv;
-    extern __shared__ int hist[];   // [R][E_loc], count blocks only
+    extern __shared__ int hist[];   // [E]: count blocks [R][E_loc] counts; token blocks expert -> entry
     const int b = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
     if (!a.packed) pdl_wait();
@@ -161,37 +163,42 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
             if (u < cunits) pre[i] = ld_stream_v4(src + (int64_t)u * 16);
         }
     }
-    // The source's earlier entries (for the slot ranks) do not depend on this token
-    // either: each thread loads its first kScanPre of them now, with the row and the
-    // token's own ids, so all three share one memory round trip.
+    // The source's entries in earlier tokens (for the slot ranks) do not depend on this
+    // token either: each thread loads its first kScanPre of them now, with the row and
+    // the token's own ids, so all three share one memory round trip.
     const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
-    const int lim = t * a.k + a.k;
+    const int lim = t * a.k;
     int64_t pre_e[kScanPre];
 #pragma unroll
     for (int q = 0; q < kScanPre; ++q) {
         const int i = threadIdx.x + q * kThreads;
         pre_e[q] = i < lim ? __ldg(tk + i) : -1;
     }
+    // hist[e] (the block's E ints, not cleared): one of this token's entries with
+    // expert e. A value left by another block is never used for an expert outside this
+    // token: a lookup counts only if the entry it names has that very expert.
     if (threadIdx.x < a.k) {
-        s_e[threadIdx.x] = a.topk_idx[tok * a.k + threadIdx.x];
+        const int64_t e = a.topk_idx[tok * a.k + threadIdx.x];
+        s_e[threadIdx.x] = e;
         s_cnt[threadIdx.x] = 0;
+        if (e >= 0 && e < a.E) hist[(int)e] = threadIdx.x;
     }
     __syncthreads();
 
-    // Rank of each entry among the source's earlier entries with the same expert.
+    // Count of the source's entries in earlier tokens with each of this token's experts,
+    // booked on the entry the table names (one shared-memory lookup per entry).
 #pragma unroll
     for (int q = 0; q < kScanPre; ++q) {
-        const int i = threadIdx.x + q * kThreads;
         const int64_t e = pre_e[q];
-        if (e < 0) continue;
-        for (int j = 0; j < a.k; ++j)
-            if (e == s_e[j] && i < t * a.k + j) atomicAdd(&s_cnt[j], 1);
+        if (e < 0 || e >= a.E) continue;
+        const int j = hist[(int)e];
+        if ((unsigned)j < (unsigned)a.k && s_e[j] == e) atomicAdd(&s_cnt[j], 1);
     }
     for (int i = threadIdx.x + kScanPre * kThreads; i < lim; i += kThreads) {
         const int64_t e = __ldg(tk + i);
-        if (e < 0) continue;
-        for (int j = 0; j < a.k; ++j)
-            if (e == s_e[j] && i < t * a.k + j) atomicAdd(&s_cnt[j], 1);
+        if (e < 0 || e >= a.E) continue;
+        const int j = hist[(int)e];
+        if ((unsigned)j < (unsigned)a.k && s_e[j] == e) atomicAdd(&s_cnt[j], 1);
     }
     __syncthreads();
     // Packed: the earlier sources' counts come from the count kernel.
@@ -202,13 +209,18 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     if (threadIdx.x < 32) {
         const int j = threadIdx.x;
         int64_t row = -1;
+        // Rank = count in earlier tokens + this token's earlier entries with the same
+        // expert (lanes >= k hold distinct values that match nothing).
+        const int64_t ej = j < a.k ? s_e[j] : -2 - (int64_t)j;
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, (unsigned long long)ej);
         if (j < a.k) {
-            const int64_t e = s_e[j];
+            const int64_t e = ej;
             int32_t pos = -1;
             if (e >= a.E || e < -1) {
                 raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
             } else if (e >= 0) {
-                if (s_cnt[j] >= a.nmax) {
+                const int rank = s_cnt[hist[(int)e]] + __popc(same & lanemask_lt());
+                if (rank >= a.nmax) {
                     raise_flag(a.err, EP_DEVERR_SLOT_OVERFLOW);
                 } else {
                     const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
                         start = 0;
                         for (int src = 0; src < s; ++src) start += a.send_count[e * a.R + src];
                     }
-                    pos = start + s_cnt[j];
+                    pos = start + rank;
                     row = ((int64_t)d * a.E_loc + el) * slots + pos;
                     a.src_info[row] = t;
                 }
@@ -392,7 +404,8 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
             // Token blocks, plus one receive-output block per destination with BOTH.
             const unsigned blocks = (unsigned)(a.R * a.T + (a.write_recv ? a.R : 0));
             if (blocks > 0)
-                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads), sizeof(int) * (size_t)a.E,
+                               launch->stream, a);
         }
         if (e != cudaSuccess) return cuda_fail(e);
     } else if (phase & EP_PHASE_SEND) {
