@@ -18,16 +18,18 @@
 // The send kernel computes that count by a block-wide scan of the source's entries in
 // earlier tokens (at most Nmax*k of them; one shared-memory lookup each, in a table from
 // expert to the token's entry), plus the token's own earlier entries with the same
-// expert (a match-any vote), so no block waits on another. Extra blocks write
-// the per-(destination, expert, source) count signals; the receive kernel only
-// reads those signals.
+// expert (a match-any vote), so no block waits on another.
 //
 // Packed variant (no gaps between the sources): entry (t, j) of source s takes
 //   sum over s' < s of count[s'][e] + (the same in-source rank),
-// so the per-source counts must exist before any row is placed. A small kernel with
-// one block per source writes them (as the count signals) and lets the send kernel
-// start at once; the send kernel loads its row and ranks its entries, then waits for
-// the counts (programmatic dependent launch) before it writes anything.
+// so the per-source counts must exist before any row is placed.
+//
+// Send phase, both layouts: a small kernel with one block per source writes the per-
+// (destination, expert, source) counts (the count signals the receive phase reads) and
+// lets the send kernel start at once; the send kernel loads its row and ranks its
+// entries, then waits for the counts (programmatic dependent launch) before it writes
+// anything. With the receive phase in the same call, R extra blocks of the send kernel
+// turn the signals into recv_expert_count / layout_range.
 #include "rowops.cuh"
 
 namespace ep {
@@ -35,7 +37,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCombineU = 1;        // units per thread per batch in the LL combine
-constexpr int kScanPre = 4;         // earlier entries per thread loaded up front (send)
+constexpr int kSendThreads = 128;   // threads per token block of the send kernel
+constexpr int kSendPre = 8;         // 16-byte row pieces per thread loaded before the scan
+constexpr int kSendScanPre = 8;     // earlier entries per thread loaded up front
 
 __device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
 
@@ -58,9 +62,10 @@ struct LLArgs {
     uint32_t* err;
 };
 
-// Packed layout, first kernel: block s counts source s's entries per expert (capped at
-// Nmax, as the send kernel caps them) into send_count[e][s]. It lets the send kernel
-// launch immediately: that kernel reads nothing of this one's before its own wait.
+// Send phase, first kernel: block s counts source s's entries per expert (capped at
+// Nmax, as the send kernel caps them) into send_count[e][s]. It waits for everything
+// earlier, then lets the send kernel launch: that kernel reads only inputs before its
+// own wait.
 __global__ void __launch_bounds__(kThreads) ll_count_kernel(LLArgs a) {
     extern __shared__ int hist[];   // [E]
     const int s = blockIdx.x;
@@ -79,66 +84,31 @@ __global__ void __launch_bounds__(kThreads) ll_count_kernel(LLArgs a) {
         a.send_count[(int64_t)e * a.R + s] = min(hist[e], a.nmax);
 }
 
-// Blocks [0, R*T): one per source token. Blocks [R*T, R*T + R): the count signals of
-// one destination rank d (sent by every source to d). When the receive phase runs in
-// the same launch (write_recv), those blocks also write recv_expert_count and
-// layout_range for d, since they already hold every count d receives.
-__global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
+// Blocks [0, R*T): one per source token. With the receive phase in the same call
+// (write_recv), blocks [R*T, R*T + R): destination d's recv_expert_count and
+// layout_range from the count kernel's signals.
+__global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
     __shared__ int64_t s_e[EP_MAX_TOPK];
     __shared__ int s_cnt[EP_MAX_TOPK];
     __shared__ int64_t s_rows[EP_MAX_TOPK];
     __shared__ int s_nv;
-    extern __shared__ int hist[];   // [E]: count blocks [R][E_loc] counts; token blocks expert -> entry
+    extern __shared__ int hist[];   // [E]: expert -> one of the token's entries
     const int b = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
-    if (!a.packed) pdl_wait();
 
-    if (b >= a.R * a.T && a.packed) {
-        // Receive outputs of destination d from the count kernel's signals.
+    if (b >= a.R * a.T) {
         const int d = b - a.R * a.T;
         pdl_wait();
-        for (int el = threadIdx.x; el < a.E_loc; el += kThreads) {
+        for (int el = threadIdx.x; el < a.E_loc; el += kSendThreads) {
             const int64_t e = (int64_t)d * a.E_loc + el;
             int start = 0;
             for (int src = 0; src < a.R; ++src) {
                 const int c = a.send_count[e * a.R + src];
-                a.layout_range[(e * a.R + src) * 2 + 0] = start;
+                a.layout_range[(e * a.R + src) * 2 + 0] = a.packed ? start : src * a.nmax;
                 a.layout_range[(e * a.R + src) * 2 + 1] = c;
                 start += c;
             }
             a.recv_expert_count[e] = start;
-        }
-        pdl_trigger();
-        return;
-    }
-    if (b >= a.R * a.T) {
-        const int d = b - a.R * a.T;
-        const int lo = d * a.E_loc;
-        for (int i = threadIdx.x; i < a.E; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        const int tk_per_src = a.T * a.k;
-#pragma unroll 8
-        for (int i = threadIdx.x; i < a.R * tk_per_src; i += kThreads) {
-            const int64_t e = __ldg(a.topk_idx + i);
-            if (e >= lo && e < lo + a.E_loc) atomicAdd(&hist[(i / tk_per_src) * a.E_loc + (int)(e - lo)], 1);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < a.E; i += kThreads) {
-            const int s = i / a.E_loc, el = i - s * a.E_loc;
-            const int c = min(hist[i], a.nmax);
-            const int64_t sig = ((int64_t)(lo + el)) * a.R + s;       // [d][el][s]
-            a.send_count[sig] = c;
-            if (a.write_recv) {
-                a.layout_range[sig * 2 + 0] = s * a.nmax;
-                a.layout_range[sig * 2 + 1] = c;
-            }
-        }
-        if (a.write_recv) {
-            for (int el = threadIdx.x; el < a.E_loc; el += kThreads) {
-                int total = 0;
-                for (int s = 0; s < a.R; ++s) total += min(hist[s * a.E_loc + el], a.nmax);
-                a.recv_expert_count[lo + el] = total;
-            }
         }
         pdl_trigger();
         return;
@@ -151,15 +121,15 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     // load overlaps the rank scan below.
     const int qunits = a.H >> 4;                 // fp8: 16 channels per unit
     const int cunits = a.H >> 3;                 // bf16 copy: 8 channels per unit
-    uint4 pre[4];
+    uint4 pre[kSendPre];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kSendPre; ++i) {
         pre[i] = make_uint4(0, 0, 0, 0);
         if (a.use_fp8) {
-            const int u = threadIdx.x + (i >> 1) * kThreads;
+            const int u = threadIdx.x + (i >> 1) * kSendThreads;
             if (u < qunits) pre[i] = ld_stream_v4(src + (int64_t)u * 32 + (i & 1) * 16);
         } else {
-            const int u = threadIdx.x + i * kThreads;
+            const int u = threadIdx.x + i * kSendThreads;
             if (u < cunits) pre[i] = ld_stream_v4(src + (int64_t)u * 16);
         }
     }
@@ -168,10 +138,10 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     // the token's own ids, so all three share one memory round trip.
     const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
     const int lim = t * a.k;
-    int64_t pre_e[kScanPre];
+    int64_t pre_e[kSendScanPre];
 #pragma unroll
-    for (int q = 0; q < kScanPre; ++q) {
-        const int i = threadIdx.x + q * kThreads;
+    for (int q = 0; q < kSendScanPre; ++q) {
+        const int i = threadIdx.x + q * kSendThreads;
         pre_e[q] = i < lim ? __ldg(tk + i) : -1;
     }
     // hist[e] (the block's E ints, not cleared): one of this token's entries with
@@ -188,21 +158,22 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     // Count of the source's entries in earlier tokens with each of this token's experts,
     // booked on the entry the table names (one shared-memory lookup per entry).
 #pragma unroll
-    for (int q = 0; q < kScanPre; ++q) {
+    for (int q = 0; q < kSendScanPre; ++q) {
         const int64_t e = pre_e[q];
         if (e < 0 || e >= a.E) continue;
         const int j = hist[(int)e];
         if ((unsigned)j < (unsigned)a.k && s_e[j] == e) atomicAdd(&s_cnt[j], 1);
     }
-    for (int i = threadIdx.x + kScanPre * kThreads; i < lim; i += kThreads) {
+    for (int i = threadIdx.x + kSendScanPre * kSendThreads; i < lim; i += kSendThreads) {
         const int64_t e = __ldg(tk + i);
         if (e < 0 || e >= a.E) continue;
         const int j = hist[(int)e];
         if ((unsigned)j < (unsigned)a.k && s_e[j] == e) atomicAdd(&s_cnt[j], 1);
     }
     __syncthreads();
-    // Packed: the earlier sources' counts come from the count kernel.
-    if (a.packed) pdl_wait();
+    // Nothing before this wait wrote: the count kernel's signals (the packed layout's
+    // earlier-source counts) are complete after it.
+    pdl_wait();
 
     // Warp 0 (k <= 32 lanes) places the entries and compacts the valid rows in entry
     // order with a ballot.
@@ -246,8 +217,8 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
     if (a.use_fp8) {
         uint8_t* q_base = reinterpret_cast<uint8_t*>(a.recv_x);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {            // the prefetched units (all lanes shuffle)
-            const int u = threadIdx.x + i * kThreads;
+        for (int i = 0; i < kSendPre / 2; ++i) { // the prefetched units (all lanes shuffle)
+            const int u = threadIdx.x + i * kSendThreads;
             float scale;
             uint32_t sbyte;
             const uint4 q = quant_unit(pre[2 * i], pre[2 * i + 1], a.qm, scale, sbyte);
@@ -255,17 +226,17 @@ __global__ void __launch_bounds__(kThreads) ll_send_kernel(LLArgs a) {
                 store_quant_unit(q_base, a.recv_x_scales, s_rows, nv, a.H, u, q, scale, sbyte, a.qm.mode);
         }
         scatter_quant_row<1>(src, q_base, a.recv_x_scales, s_rows, nv, a.H, a.qm, threadIdx.x,
-                             kThreads, 2 * kThreads);
+                             kSendThreads, kSendPre / 2 * kSendThreads);
     } else {
         for (int p = 0; p < nv; ++p) {
             char* dst = a.recv_x + s_rows[p] * (int64_t)a.H * 2;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int u = threadIdx.x + i * kThreads;
+            for (int i = 0; i < kSendPre; ++i) {
+                const int u = threadIdx.x + i * kSendThreads;
                 if (u < cunits) st_v4(dst + (int64_t)u * 16, pre[i]);
             }
         }
-        for (int u = threadIdx.x + 4 * kThreads; u < cunits; u += kThreads) {
+        for (int u = threadIdx.x + kSendPre * kSendThreads; u < cunits; u += kSendThreads) {
             const uint4 v = ld_stream_v4(src + (int64_t)u * 16);
             for (int p = 0; p < nv; ++p) st_v4(a.recv_x + s_rows[p] * (int64_t)a.H * 2 + (int64_t)u * 16, v);
         }
@@ -397,21 +368,16 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;
-    if ((phase & EP_PHASE_SEND) && a.packed) {
+    if (phase & EP_PHASE_SEND) {
         cudaError_t e = launch_pdl(ll_count_kernel, dim3((unsigned)a.R), dim3(kThreads),
                                    sizeof(int) * (size_t)a.E, launch->stream, a);
         if (e == cudaSuccess) {
             // Token blocks, plus one receive-output block per destination with BOTH.
             const unsigned blocks = (unsigned)(a.R * a.T + (a.write_recv ? a.R : 0));
             if (blocks > 0)
-                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads), sizeof(int) * (size_t)a.E,
+                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kSendThreads), sizeof(int) * (size_t)a.E,
                                launch->stream, a);
         }
-        if (e != cudaSuccess) return cuda_fail(e);
-    } else if (phase & EP_PHASE_SEND) {
-        const unsigned blocks = (unsigned)(a.R * a.T + a.R);
-        cudaError_t e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kThreads),
-                                   sizeof(int) * (size_t)a.E, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (phase == EP_PHASE_RECV) {
