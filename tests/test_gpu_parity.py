@@ -216,6 +216,10 @@ LL_CASES = {
     "tiny": W("lt", R=2, T=128, H=256, E=8, k=2, nmax=128, seed=0),
     "masked": W("lm", R=4, T=40, H=512, E=32, k=6, nmax=48, mask_p=0.05, seed=111),
     "r8": W("l8", R=8, T=100, H=1024, E=64, k=8, nmax=128, mask_p=0.05, seed=112),
+    # more earlier entries than a send block loads up front (t*k > 1024)
+    "long": W("ll", R=2, T=300, H=256, E=16, k=8, nmax=300, mask_p=0.05, seed=118),
+    # rows longer than a send block loads up front (bf16 > 16 KB, e4m3 source > 16 KB)
+    "wide": W("lw", R=2, T=20, H=16384, E=8, k=4, nmax=24, seed=119),
 }
 
 
