@@ -216,8 +216,8 @@ typedef struct ep_recv {
  *   EP_LL_LAYOUT_PACKED  no gaps: the expert's rows are 0 .. recv_expert_count-1 in
  *                        (source, token) order, source s starting at the sum of the
  *                        counts of sources s' < s, so a grouped GEMM reads one
- *                        contiguous block per expert. The send phase then takes two
- *                        kernels (a per-source count, then the rows). */
+ *                        contiguous block per expert.
+ * Either layout's send phase is two kernels: a per-source count, then the rows. */
 typedef enum ep_ll_layout { EP_LL_LAYOUT_SLOTS = 0, EP_LL_LAYOUT_PACKED = 1 } ep_ll_layout;
 
 /* Low-latency buffers and handle ([README] low-latency example; [HOOK]). All dev.
@@ -262,7 +262,7 @@ EP_API size_t ep_layout_workspace_size(const ep_shape* shape);
  *   handle    every field except recv_src_idx is written (recv_src_idx is ignored).
  *   workspace dev, >= ep_layout_workspace_size bytes, 16-byte aligned; contents need
  *             no initialisation and are overwritten.
- * Two kernels (four with the expert-major placement), no host synchronisation. Bad
+ * Two kernels (three with the expert-major placement), no host synchronisation. Bad
  * entries: EP_DEVERR_BAD_EXPERT. */
 EP_API ep_status ep_get_layout(const ep_shape* shape, const int64_t* topk_idx, ep_layout* layout,
                         ep_handle* handle, void* workspace, size_t workspace_bytes,
@@ -386,7 +386,8 @@ EP_API ep_status ep_combine_expert_major(const ep_shape* shape, const void* y,
  * signals into recv_expert_count and layout_range; EP_PHASE_BOTH does both. A hook
  * is the caller issuing the RECV call later (there is no stored closure in a C ABI).
  *   x        dev [R][T][H] bf16; T <= Nmax is required
- *   topk_idx dev [R][T][k] int64 (-1 masked); experts of one token must be distinct
+ *   topk_idx dev [R][T][k] int64 (-1 masked); a repeated expert within a token takes
+ *            one slot per entry, in entry order
  *   buf      see ep_ll_buffer (recv_x_scales required iff use_fp8)
  * Slot overflow: EP_DEVERR_SLOT_OVERFLOW; bad experts: EP_DEVERR_BAD_EXPERT. */
 EP_API ep_status ep_ll_dispatch(const ep_shape* shape, const void* x, const int64_t* topk_idx,
