@@ -383,7 +383,7 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
     if (phase == EP_PHASE_RECV) {
         // Receive phase launched on its own (the hook): turn the count signals written
         // by the send phase into counts and layout ranges. With EP_PHASE_BOTH the send
-        // kernel's count blocks already wrote them.
+        // kernel's extra blocks already wrote them.
         cudaError_t e = launch_pdl(ll_recv_kernel, dim3((unsigned)ceil_div(a.E, kThreads)),
                                    dim3(kThreads), 0, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
