@@ -91,6 +91,10 @@ class LayoutBuffers:
                          _ptr(self.num_recv_tokens_per_expert), _ptr(self.expert_rows),
                          _ptr(self.expert_prefix))
 
+    def tensors(self) -> list:
+        """Every device tensor this object owns."""
+        return [v for v in vars(self).values() if isinstance(v, torch.Tensor)]
+
     def as_dict(self) -> dict:
         return {k: getattr(self, k) for k in (
             "num_tokens_per_rank", "num_tokens_per_expert", "is_token_in_rank",
@@ -153,6 +157,10 @@ class LLBuffers:
         if fill is not None:
             self.recv_x.view(torch.uint8).fill_(fill)
             self.src_info.fill_(-7)
+
+    def tensors(self) -> list:
+        """Every device tensor this object owns."""
+        return [v for v in vars(self).values() if isinstance(v, torch.Tensor)]
 
     def struct(self) -> ep_ll_buffer:
         return ep_ll_buffer(_ptr(self.recv_x), _ptr(self.recv_x_scales), _ptr(self.src_info),

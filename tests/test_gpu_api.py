@@ -156,3 +156,42 @@ def test_buffer_expert_major_blocks():
                                       em["expert_rows"], np.array(off), W.E, weighted=True)
     assert_close_bf16(host_bits(out), ref)
     assert buf.check_errors() == 0
+
+
+def test_buffer_comm_stream_events_and_helpers():
+    """The calls run on the Buffer's comm stream after a captured event; with
+    async_finish the compute stream waits only through the returned event. Also the
+    size hint and clean_low_latency_buffer helpers."""
+    inp, x, topk, wts = _inputs()
+    buf = Buffer(W.R, W.E, W.H, W.k, W.C)
+    assert buf.get_comm_stream() != torch.cuda.current_stream()
+    prev = Buffer.capture()
+    recv_x, _, _, _, handle, ev = buf.dispatch(x, topk_idx=topk, topk_weights=wts, num_worst_tokens=True,
+                                               previous_event=prev, async_finish=True,
+                                               allocate_on_comm_stream=True)
+    ev.current_stream_wait()
+    ref = oracle.layout(inp["topk_idx"], W.E, W.C)
+    off = handle.row_offset
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), W.E)
+    counts = ref["rank_prefix_matrix"][-1]
+    for d in range(W.R):
+        n = int(counts[d])
+        np.testing.assert_array_equal(host_bits(recv_x[d])[:n], exp["recv_x"][off[d]:off[d] + n])
+    # a combine chained on the dispatch's event, without async_finish: the compute stream
+    # waits for it before the copy to the host
+    out, _, _ = buf.combine(recv_x, handle, previous_event=ev, weight_by=(topk, wts))
+    ec = oracle.combine(exp["recv_x"], ref["send_head"], np.array(off), W.E, W.k,
+                        oracle.COMBINE_WEIGHTED, inp["topk_idx"], inp["topk_weights"])
+    assert_close_bf16(host_bits(out), ec["out"])
+
+    hint = buf.get_buffer_size_hint(W.T, fp8=True, num_max_dispatch_tokens_per_rank=W.T)
+    assert hint["recv_rows"] == W.R * W.R * W.T
+    w = workloads.Workload("apic", R=4, T=16, H=256, E=16, k=4, mask_p=0.0, nmax=16, seed=504)
+    _, xl, tl, _ = _inputs(w)
+    bl = Buffer(w.R, w.E, w.H, w.k)
+    _, count, lh, _, _ = bl.low_latency_dispatch(xl, tl, w.nmax, use_fp8=True)
+    assert int(count.sum().item()) == w.R * w.T * w.k
+    bl.clean_low_latency_buffer(lh)
+    assert int(lh.buf.recv_expert_count.abs().sum().item()) == 0
+    assert int(lh.buf.send_count.abs().sum().item()) == 0
+    assert buf.check_errors() == 0 and bl.check_errors() == 0
