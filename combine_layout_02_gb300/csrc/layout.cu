@@ -358,6 +358,22 @@ __global__ void __launch_bounds__(kThreads) layout_expert_rows_kernel(LayoutArgs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_trigger();
     pdl_wait();
+    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
+    const int lt = threadIdx.x;
+    // Loads that do not depend on one another go out together, before any barrier: the
+    // first tile's ids (k <= 8: kept in registers for both passes over the tile) and this
+    // block's column prefixes (E <= threads per block).
+    const bool keep_ids = a.k <= 8;
+    int64_t ev0[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ev0[i] = -1;
+    if (keep_ids && lt < sub && t0 + lt < t1) {
+        const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t0 + lt) * a.k;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < a.k) ev0[i] = __ldg(row + i);
+    }
+    const int col = (a.E <= kThreads && lt < a.E) ? a.ws_expert[((int64_t)s * a.C + c) * a.E + lt] : 0;
     // Per destination d (one warp each): exclusive prefix of the expert totals over its
     // local experts -> running[e]; block (0, 0) also writes expert_prefix.
     for (int d = warp; d < a.R; d += kWarps) {
@@ -380,10 +396,12 @@ __global__ void __launch_bounds__(kThreads) layout_expert_rows_kernel(LayoutArgs
         if (c == 0 && s == 0 && lane == 0) a.expert_prefix[(int64_t)d * (a.E_loc + 1) + a.E_loc] = carry;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += kThreads)
-        running[e] += a.ws_expert[((int64_t)s * a.C + c) * a.E + e];
-    const int t0 = min(c * a.tpc, a.T), t1 = min(t0 + a.tpc, a.T);
-    const int lt = threadIdx.x;
+    if (a.E <= kThreads) {
+        if (lt < a.E) running[lt] += col;
+    } else {
+        for (int e = threadIdx.x; e < a.E; e += kThreads)
+            running[e] += a.ws_expert[((int64_t)s * a.C + c) * a.E + e];
+    }
     for (int base = t0; base < t1; base += sub) {   // block-uniform trip count
         for (int i = threadIdx.x; i < a.E * WS; i += kThreads) mask[i] = 0u;
         __syncthreads();
@@ -391,10 +409,12 @@ __global__ void __launch_bounds__(kThreads) layout_expert_rows_kernel(LayoutArgs
         const bool mine = lt < sub && t < t1;
         const int64_t* row = a.topk_idx + ((int64_t)s * a.T + t) * a.k;
         // The token's ids are loaded in batches of 8 before any shared-memory atomic.
+        const bool first = keep_ids && base == t0;
         for (int j0 = 0; j0 < a.k; j0 += 8) {
             int64_t ev[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ev[i] = (mine && j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+            for (int i = 0; i < 8; ++i)
+                ev[i] = first ? ev0[i] : ((mine && j0 + i < a.k) ? __ldg(row + j0 + i) : -1);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if (ev[i] >= 0 && ev[i] < a.E) atomicOr(&mask[ev[i] * WS + (lt >> 5)], 1u << (lt & 31));
@@ -403,7 +423,8 @@ __global__ void __launch_bounds__(kThreads) layout_expert_rows_kernel(LayoutArgs
         for (int j0 = 0; j0 < a.k; j0 += 8) {
             int64_t ev[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ev[i] = (mine && j0 + i < a.k) ? __ldg(row + j0 + i) : -1;
+            for (int i = 0; i < 8; ++i)
+                ev[i] = first ? ev0[i] : ((mine && j0 + i < a.k) ? __ldg(row + j0 + i) : -1);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 if (!mine || j0 + i >= a.k) continue;
