@@ -62,6 +62,35 @@ struct LLArgs {
     uint32_t* err;
 };
 
+// Receive outputs of expert e, by one warp: lane s (and s + 32) loads the count signal of
+// source s, so all of them go out at once; a shuffle scan over the lanes gives the packed
+// layout's starts. layout_range[e][s] = (first slot of source s, count), recv_expert_count[e]
+// = the sum.
+__device__ __forceinline__ void expert_ranges_warp(const LLArgs& a, int64_t e, int lane) {
+    const int c0 = lane < a.R ? a.send_count[e * a.R + lane] : 0;
+    const int c1 = lane + 32 < a.R ? a.send_count[e * a.R + lane + 32] : 0;
+    int i0 = c0, i1 = c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y0 = __shfl_up_sync(0xFFFFFFFFu, i0, o);
+        const int y1 = __shfl_up_sync(0xFFFFFFFFu, i1, o);
+        if (lane >= o) {
+            i0 += y0;
+            i1 += y1;
+        }
+    }
+    const int t0 = __shfl_sync(0xFFFFFFFFu, i0, 31), t1 = __shfl_sync(0xFFFFFFFFu, i1, 31);
+    if (lane < a.R) {
+        a.layout_range[(e * a.R + lane) * 2 + 0] = a.packed ? i0 - c0 : lane * a.nmax;
+        a.layout_range[(e * a.R + lane) * 2 + 1] = c0;
+    }
+    if (lane + 32 < a.R) {
+        a.layout_range[(e * a.R + lane + 32) * 2 + 0] = a.packed ? t0 + i1 - c1 : (lane + 32) * a.nmax;
+        a.layout_range[(e * a.R + lane + 32) * 2 + 1] = c1;
+    }
+    if (lane == 0) a.recv_expert_count[e] = t0 + t1;
+}
+
 // Send phase, first kernel: block s counts source s's entries per expert (capped at
 // Nmax, as the send kernel caps them) into send_count[e][s]. It waits for everything
 // earlier, then lets the send kernel launch: that kernel reads only inputs before its
@@ -99,17 +128,8 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
     if (b >= a.R * a.T) {
         const int d = b - a.R * a.T;
         pdl_wait();
-        for (int el = threadIdx.x; el < a.E_loc; el += kSendThreads) {
-            const int64_t e = (int64_t)d * a.E_loc + el;
-            int start = 0;
-            for (int src = 0; src < a.R; ++src) {
-                const int c = a.send_count[e * a.R + src];
-                a.layout_range[(e * a.R + src) * 2 + 0] = a.packed ? start : src * a.nmax;
-                a.layout_range[(e * a.R + src) * 2 + 1] = c;
-                start += c;
-            }
-            a.recv_expert_count[e] = start;
-        }
+        for (int el = threadIdx.x >> 5; el < a.E_loc; el += kSendThreads / 32)
+            expert_ranges_warp(a, (int64_t)d * a.E_loc + el, threadIdx.x & 31);
         pdl_trigger();
         return;
     }
@@ -244,20 +264,12 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
     pdl_trigger();
 }
 
-// One thread per (destination rank, local expert) = expert e.
+// One warp per (destination rank, local expert) = expert e.
 __global__ void __launch_bounds__(kThreads) ll_recv_kernel(LLArgs a) {
-    const int e = blockIdx.x * kThreads + threadIdx.x;
+    const int64_t e = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     pdl_trigger();
     pdl_wait();
-    if (e >= a.E) return;
-    int total = 0;
-    for (int s = 0; s < a.R; ++s) {
-        const int c = a.send_count[(int64_t)e * a.R + s];
-        a.layout_range[((int64_t)e * a.R + s) * 2 + 0] = a.packed ? total : s * a.nmax;
-        a.layout_range[((int64_t)e * a.R + s) * 2 + 1] = c;
-        total += c;
-    }
-    a.recv_expert_count[e] = total;
+    if (e < a.E) expert_ranges_warp(a, e, threadIdx.x & 31);
 }
 
 // One block per output token: weighted sum over the token's valid entries.
@@ -384,7 +396,7 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
         // Receive phase launched on its own (the hook): turn the count signals written
         // by the send phase into counts and layout ranges. With EP_PHASE_BOTH the send
         // kernel's extra blocks already wrote them.
-        cudaError_t e = launch_pdl(ll_recv_kernel, dim3((unsigned)ceil_div(a.E, kThreads)),
+        cudaError_t e = launch_pdl(ll_recv_kernel, dim3((unsigned)ceil_div(a.E, kThreads / 32)),
                                    dim3(kThreads), 0, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }
