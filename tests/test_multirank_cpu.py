@@ -70,3 +70,31 @@ def test_every_bench_workload_resolves():
     for name in bench.WORKLOAD_TEXT:
         w = bench.workload_config(name)
         assert w.E % w.R == 0 and w.H % 128 == 0
+
+
+def test_roofline_traffic_only_for_its_own_workload_and_sources():
+    """The committed DRAM counters are reported only for the workload and the kernel
+    sources they were taken on; any other workload reads as null."""
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        entries = json.load(f)
+    for kernel in bench.KERNEL_SOURCES:
+        e = entries[kernel]
+        got = bench.traffic_from_profiles(kernel, e.get("workload", "dsv3"))
+        current = e["source_sha256"] == bench.source_digest(bench.KERNEL_SOURCES[kernel])
+        assert got == (e["dram_bytes_per_launch"] if current else None)
+        assert bench.traffic_from_profiles(kernel, "zipf_reuse") is None
+    assert bench.traffic_from_profiles("ll_combine_kernel") is None
+
+
+def test_fp8_scale_names_match_the_abi():
+    sys.path.insert(0, ROOT)
+    import bench
+    import combine_layout_02_gb300 as ep
+    assert bench.FP8_SCALE == {"fp32": ep.EP_FP8_SCALE_FP32, "pow2": ep.EP_FP8_SCALE_POW2,
+                               "ue8m0": ep.EP_FP8_SCALE_UE8M0, "tensor": ep.EP_FP8_SCALE_TENSOR}
+    # every phase a workload can time names the kernel its roofline would cite
+    assert {"combine_backward", "dispatch_backward", "dispatch", "dispatch_fp8", "combine",
+            "dispatch_em", "combine_em", "ll_send", "ll_recv", "ll_combine"} <= set(bench.PHASE_KERNEL)
