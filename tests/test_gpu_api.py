@@ -195,3 +195,26 @@ def test_buffer_comm_stream_events_and_helpers():
     assert int(lh.buf.recv_expert_count.abs().sum().item()) == 0
     assert int(lh.buf.send_count.abs().sum().item()) == 0
     assert buf.check_errors() == 0 and bl.check_errors() == 0
+
+
+def test_buffer_comm_stream_follows_a_delayed_compute_stream():
+    """Without previous_event the comm stream waits for the work already issued on the
+    compute stream: x is written there after a bounded busy kernel, and the dispatch on
+    the comm stream still sees the final x."""
+    inp, x, topk, wts = _inputs()
+    buf = Buffer(W.R, W.E, W.H, W.k, W.C)
+    x2 = torch.zeros_like(x)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(20_000_000)          # keep the compute stream busy (bounded)
+    x2.copy_(x)
+    recv_x, _, _, _, handle, ev = buf.dispatch(x2, topk_idx=topk, num_worst_tokens=True,
+                                               async_finish=True)
+    ev.current_stream_wait()
+    ref = oracle.layout(inp["topk_idx"], W.E, W.C)
+    off = handle.row_offset
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), W.E)
+    counts = ref["rank_prefix_matrix"][-1]
+    for d in range(W.R):
+        n = int(counts[d])
+        np.testing.assert_array_equal(host_bits(recv_x[d])[:n], exp["recv_x"][off[d]:off[d] + n])
+    assert buf.check_errors() == 0
