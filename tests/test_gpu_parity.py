@@ -588,3 +588,24 @@ def test_clean_ll_buffer_zeroes_the_signals_and_counts():
     counts = ep.ep_read_recv_counts_sync(run3.sh, run3.lb.handle())
     np.testing.assert_array_equal(counts, ref["rank_prefix_matrix"][-1])
     assert run.flags() == 0
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("use_fp8", [False, True])
+def test_ll_repeated_experts_bit_exact(packed, use_fp8):
+    """Tokens that name an expert more than once (no overflow): every entry gets its own
+    slot in entry order, exactly as the oracle places it."""
+    rng = np.random.default_rng(121)
+    R, T, H, E, k, nmax = 2, 30, 256, 4, 3, 128
+    topk = rng.integers(-1, E, size=(R, T, k)).astype(np.int64)
+    inp = {"x": workloads.make_hidden(rng, R, T, H), "topk_idx": topk,
+           "topk_weights": np.full((R, T, k), 1.0 / k, np.float32)}
+    run = GpuRun(R, T, H, E, k, 1, inp, nmax=nmax)
+    buf = run.ll_dispatch(use_fp8, packed=packed)
+    exp = oracle.ll_dispatch(inp["x"], topk, E, nmax, use_fp8, packed=packed,
+                             fill_x=0x5A5A if not use_fp8 else 0x5A)
+    assert exp["bad_entries"] == 0
+    for key in ("slot", "recv_expert_count", "layout_range", "src_info"):
+        np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
+    np.testing.assert_array_equal(host_bits(buf.recv_x), exp["recv_x"])
+    assert run.flags() == 0

@@ -222,3 +222,34 @@ def test_ll_packed_combine_equals_slot_layout_combine():
     a = oracle.ll_combine(ys, topk, inp["topk_weights"], sl["slot"], w.E, w.nmax)
     b = oracle.ll_combine(yp, topk, inp["topk_weights"], pk["slot"], w.E, w.nmax)
     np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("packed", [False, True])
+def test_ll_repeated_experts_take_one_slot_per_entry_in_entry_order(packed):
+    """A token may name an expert twice: each entry takes its own slot, ranked by entry
+    order (token, then k) among the source's entries with that expert (brute force)."""
+    rng = np.random.default_rng(57)
+    R, T, k, E, nmax = 2, 6, 3, 4, 40
+    topk = rng.integers(-1, E, size=(R, T, k)).astype(np.int64)
+    assert any(len(set(r[r >= 0].tolist())) < int((r >= 0).sum()) for r in topk.reshape(-1, k))
+    x = workloads.make_hidden(rng, R, T, 128)
+    res = oracle.ll_dispatch(x, topk, E, nmax, False, packed=packed)
+    assert res["bad_entries"] == 0
+    E_loc = E // R
+    counts = np.array([[int(np.sum(topk[s] == e)) for s in range(R)] for e in range(E)])
+    for s in range(R):
+        seen = {}
+        for t in range(T):
+            for j in range(k):
+                e = int(topk[s, t, j])
+                if e < 0:
+                    assert res["slot"][s, t, j] == -1
+                    continue
+                r = seen.get(e, 0)
+                seen[e] = r + 1
+                start = int(counts[e, :s].sum()) if packed else s * nmax
+                assert res["slot"][s, t, j] == start + r
+                d, el = divmod(e, E_loc)
+                assert res["src_info"][d, el, start + r] == t
+                np.testing.assert_array_equal(res["recv_x"][d, el, start + r], x[s, t])
+    np.testing.assert_array_equal(res["recv_expert_count"].reshape(-1), counts.sum(1))
