@@ -116,6 +116,41 @@ def test_invalid_arguments_rejected_on_host(ep):
     st = L.ep_ll_dispatch(ctypes.byref(sh_ll2), 0x7000, 0x8000, 0, ep.EP_PHASE_SEND,
                           ctypes.byref(buf_l), ctypes.byref(launch))
     assert st == ep.EP_ERR_INVALID_ARG        # unknown receive layout
+    # expert-major: no expert_rows in the handle, recv_topk_idx given (one entry per row),
+    # a scale format without e4m3, too many experts
+    off4 = (ctypes.c_int64 * 3)(0, 8, 16)
+    oe = ep.ep_recv(0x2000, None, None, None, None, ctypes.cast(off4, ctypes.c_void_p))
+    st = L.ep_dispatch_expert_major(ctypes.byref(sh), 0x3000, ep.EP_BF16, 0x4000, None,
+                                    ctypes.byref(ep.ep_handle()), ctypes.byref(oe), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    he = ep.ep_handle()
+    he.expert_rows = 0x1000
+    he.expert_prefix = 0x1800
+    oe_bad = ep.ep_recv(0x2000, None, 0x2400, None, None, ctypes.cast(off4, ctypes.c_void_p))
+    st = L.ep_dispatch_expert_major(ctypes.byref(sh), 0x3000, ep.EP_BF16, 0x4000, None,
+                                    ctypes.byref(he), ctypes.byref(oe_bad), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    oe_fmt = ep.ep_recv(0x2000, None, None, None, None, ctypes.cast(off4, ctypes.c_void_p),
+                        ep.ep_fp8_options(ep.EP_FP8_SCALE_UE8M0, 0.0))
+    st = L.ep_dispatch_expert_major(ctypes.byref(sh), 0x3000, ep.EP_BF16, 0x4000, None,
+                                    ctypes.byref(he), ctypes.byref(oe_fmt), ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    many = ep.make_shape(2, 4, 128, ep.EP_EXPERT_MAJOR_MAX_EXPERTS * 2, 2)
+    st = L.ep_dispatch_expert_major(ctypes.byref(many), 0x3000, ep.EP_BF16, 0x4000, None,
+                                    ctypes.byref(he), ctypes.byref(oe), ctypes.byref(launch))
+    assert st == ep.EP_ERR_UNSUPPORTED
+    # expert-major combine: weighted without weights, unknown mode
+    for mode, w in ((ep.EP_COMBINE_WEIGHTED, None), (5, 0x5000)):
+        st = L.ep_combine_expert_major(ctypes.byref(sh), 0x3000, ctypes.cast(off4, ctypes.c_void_p),
+                                       ctypes.byref(he), mode, 0x4000, w, 0x6000, ctypes.byref(launch))
+        assert st == ep.EP_ERR_INVALID_ARG, mode
+    # low-latency combine: misaligned output, bad phase
+    st = L.ep_ll_combine(ctypes.byref(sh_ll2), 0x3000, 0x4000, 0x5000, ctypes.byref(buf),
+                         ep.EP_PHASE_BOTH, 0x6008, ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
+    st = L.ep_ll_combine(ctypes.byref(sh_ll2), 0x3000, 0x4000, 0x5000, ctypes.byref(buf),
+                         8, 0x6000, ctypes.byref(launch))
+    assert st == ep.EP_ERR_INVALID_ARG
     # unsupported shape
     big = ep.make_shape(65, 4, 128, 65, 1)
     st = L.ep_dispatch(ctypes.byref(big), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,
