@@ -32,6 +32,23 @@ def assert_close_bf16(got_bits, exp_bits, atol=ATOL, rtol=RTOL):
     assert not bad.any(), f"{bad.sum()} elements outside tolerance; first at {np.argwhere(bad)[0]}"
 
 
+def assert_close_bf16_dev(got: torch.Tensor, exp_bits: np.ndarray, atol=ATOL, rtol=RTOL,
+                          chunk=1 << 24):
+    """assert_close_bf16 for a device bf16 tensor against expected bf16 bit patterns,
+    evaluated on the device in float64 chunk by chunk (full-size outputs)."""
+    g_all = got.reshape(-1)
+    e_all = np.ascontiguousarray(exp_bits).reshape(-1)
+    assert g_all.numel() == e_all.size, (g_all.numel(), e_all.size)
+    for i in range(0, e_all.size, chunk):
+        e = torch.from_numpy(e_all[i:i + chunk].view(np.int16)).cuda().view(torch.bfloat16).double()
+        g = g_all[i:i + chunk].double()
+        bad = (g - e).abs() > atol + rtol * e.abs()
+        if bool(bad.any()):
+            first = i + int(torch.nonzero(bad)[0].item())
+            raise AssertionError(f"{int(bad.sum().item())} elements outside tolerance in chunk at "
+                                 f"{i}; first at flat index {first}")
+
+
 def compact_offsets(rank_prefix: np.ndarray) -> list:
     off = [0]
     for n in rank_prefix[-1]:

@@ -11,9 +11,10 @@ Checks: every layout / handle tensor bit-exact against the oracle at full size; 
 received row equal to its source row at the oracle's mapping (a device-side gather over
 all rows) and every unmapped row still holding its canary; receive metadata bit-exact
 against the oracle run at full size with a narrow hidden size (metadata does not depend
-on H); FP8 bytes and scales bit-exact on sampled tokens against the oracle quantiser;
-combine output against the oracle pipeline on a token subset (per-token results do not
-depend on the other tokens).
+on H); FP8 bytes and scales of every received row bit-exact against the oracle's
+quantisation of every source token; every combined token against the oracle's own
+layout -> dispatch -> combine pipeline over the whole workload (compared on the device,
+within the combine tolerance).
 """
 import numpy as np
 import pytest
@@ -22,11 +23,9 @@ import torch
 import combine_layout_02_gb300 as ep
 import oracle
 import workloads
-from gpu_util import GpuRun, assert_close_bf16, dev_bf16, host_bits
+from gpu_util import GpuRun, assert_close_bf16, assert_close_bf16_dev, dev_bf16, host_bits
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
-
-SUB = 96          # tokens per source rank in the oracle subsets
 
 
 def _run(name):
@@ -65,14 +64,36 @@ def _layout_and_compare(run, w, inp):
     return ref
 
 
-def _subset_pipeline(w, inp, Ts, weighted=True):
-    sub = {k: np.ascontiguousarray(v[:, :Ts]) for k, v in inp.items()}
-    lay = oracle.layout(sub["topk_idx"], w.E, w.C)
+def _oracle_pipeline(w, inp, weighted=True):
+    """The oracle's layout -> dispatch (exact regions) -> combine over every token of the
+    workload: the expected combine output of identity experts."""
+    lay = oracle.layout(inp["topk_idx"], w.E, w.C)
     off = np.concatenate([[0], np.cumsum(lay["rank_prefix_matrix"][-1])]).astype(np.int64)
-    d = oracle.dispatch(sub["x"], lay["send_head"], off, w.E)
+    d = oracle.dispatch(inp["x"], lay["send_head"], off, w.E)
     mode = oracle.COMBINE_WEIGHTED if weighted else oracle.COMBINE_SUM
-    return oracle.combine(d["recv_x"], lay["send_head"], off, w.E, w.k, mode, sub["topk_idx"],
-                          sub["topk_weights"])["out"]
+    out = oracle.combine(d["recv_x"], lay["send_head"], off, w.E, w.k, mode, inp["topk_idx"],
+                         inp["topk_weights"])["out"]
+    del d
+    return out
+
+
+def _check_fp8_rows(recv_x, recv_x_scales, exp_q, exp_s, rows, rows_exp, total_rows, canary_byte,
+                    chunk=16384):
+    """Every received e4m3 row and scale row (rows, in the GPU's regions) equals the
+    oracle dispatch's row (rows_exp, in the oracle's regions); unmapped rows keep the
+    canary byte and NaN scales."""
+    q_d = torch.from_numpy(np.ascontiguousarray(exp_q)).cuda()
+    s_d = torch.from_numpy(np.ascontiguousarray(exp_s).view(np.int32)).cuda()
+    rows_t = torch.from_numpy(rows).cuda()
+    exp_t = torch.from_numpy(rows_exp).cuda()
+    for i in range(0, len(rows), chunk):
+        r, e = rows_t[i:i + chunk], exp_t[i:i + chunk]
+        assert torch.equal(recv_x[r], q_d[e]), f"e4m3 bytes differ in chunk {i}"
+        assert torch.equal(recv_x_scales[r].view(torch.int32), s_d[e]), f"scales differ in chunk {i}"
+    mapped = torch.zeros(total_rows, dtype=torch.bool, device="cuda")
+    mapped[rows_t] = True
+    assert bool((recv_x[~mapped] == canary_byte).all()), "an unmapped row was written"
+    assert bool(torch.isnan(recv_x_scales[~mapped]).all()), "an unmapped scale row was written"
 
 
 def _metadata_reference(w, inp, ref, off):
@@ -97,8 +118,7 @@ def test_dsv3_full_size():
     np.testing.assert_array_equal(host_bits(rb.recv_topk_weights).view(np.uint32),
                                   meta["recv_topk_weights"].view(np.uint32))
     out, _ = run.combine(rb.recv_x, off, ep.EP_COMBINE_WEIGHTED)
-    exp = _subset_pipeline(w, inp, SUB)
-    assert_close_bf16(host_bits(out[:, :SUB]), exp)
+    assert_close_bf16_dev(out, _oracle_pipeline(w, inp))
     assert run.flags() == 0
 
 
@@ -108,28 +128,19 @@ def test_group_limited_fp8_full_size():
     assert (ref["is_token_in_rank"].sum(-1) <= 4).all()        # group-limited: <= 4 ranks
     off = [int(v) for v in workloads.worst_case_row_offsets(w.R, w.T)]
     rb = run.dispatch(off, recv_dtype=ep.EP_FP8_E4M3)
-    rows, toks = _mapping(ref["send_head"], off)
-    # sampled tokens: bytes and scales equal the oracle's quantisation of the source row
-    rng = np.random.default_rng(7)
-    pick = rng.choice(len(rows), 3000, replace=False)
-    q, sc = oracle.quantize_rows(inp["x"].reshape(-1, w.H)[toks[pick]])
-    got_q = rb.recv_x[torch.from_numpy(rows[pick]).cuda()].cpu().numpy()
-    got_s = rb.recv_x_scales[torch.from_numpy(rows[pick]).cuda()].cpu().numpy()
-    np.testing.assert_array_equal(got_q, q)
-    np.testing.assert_array_equal(got_s.view(np.uint32), sc.view(np.uint32))
-    # every row of a token holds the same bytes (quantised once): compare with the row of
-    # the token's first destination, for all rows
-    first = {}
-    ref_rows = np.empty_like(rows)
-    for i, t in enumerate(toks):
-        ref_rows[i] = first.setdefault(int(t), int(rows[i]))
-    r_t, f_t = torch.from_numpy(rows).cuda(), torch.from_numpy(ref_rows).cuda()
-    assert torch.equal(rb.recv_x[r_t], rb.recv_x[f_t])
-    assert torch.equal(rb.recv_x_scales[r_t], rb.recv_x_scales[f_t])
-    # bf16 combine of the bf16 rows
+    rows, _ = _mapping(ref["send_head"], off)
+    # every received row: bytes and scales equal the oracle's FP8 dispatch of the same
+    # routing (into exact regions; rows_c are the same entries' rows there)
+    off_c = np.concatenate([[0], np.cumsum(ref["rank_prefix_matrix"][-1])]).astype(np.int64)
+    rows_c, _ = _mapping(ref["send_head"], off_c)
+    exp = oracle.dispatch(inp["x"], ref["send_head"], off_c, w.E, x_kind=oracle.X_QUANTIZE)
+    _check_fp8_rows(rb.recv_x, rb.recv_x_scales, exp["recv_x"], exp["recv_x_scales"], rows, rows_c,
+                    off[-1], 0xA5)
+    del exp
+    # bf16 combine of the bf16 rows, every token
     rb16 = run.dispatch(off)
     out, _ = run.combine(rb16.recv_x, off, ep.EP_COMBINE_WEIGHTED)
-    assert_close_bf16(host_bits(out[:, :SUB]), _subset_pipeline(w, inp, SUB))
+    assert_close_bf16_dev(out, _oracle_pipeline(w, inp))
     assert run.flags() == 0
 
 
@@ -171,8 +182,7 @@ def test_zipf_handle_reuse_full_size():
         out, _ = run.combine(rb.recv_x, off, ep.EP_COMBINE_WEIGHTED)
         if it in (0, 9):
             _check_rows_gather(rb.recv_x, xd.view(-1, w.H), rows, toks, off[-1], 0xA5)
-            sub_inp = dict(inp, x=x_it)
-            assert_close_bf16(host_bits(out[:, :SUB]), _subset_pipeline(w, sub_inp, SUB))
+            assert_close_bf16_dev(out, _oracle_pipeline(w, dict(inp, x=x_it)))
     assert run.flags() == 0
 
 
