@@ -184,10 +184,16 @@ class Buffer:
     def _end(self, call: _Call, keep=()) -> EventOverlap:
         """Marks the tensors the call touched as in use on its stream (so the caching
         allocator does not hand them out again before its kernels are done) and, without
-        async_finish, makes the compute stream wait for the call."""
+        async_finish, makes the compute stream wait for the call. Outputs allocated from
+        the comm stream's pool are read on the compute stream, so they are also marked as
+        in use there: freeing them then waits for the compute stream's work issued so far
+        before the block can serve another comm-stream call (one that passes an older
+        previous_event does not wait for the compute stream itself)."""
         if call.stream is not call.compute:
             for t in call.tensors:
                 t.record_stream(call.stream)
+                if call.on_comm_alloc:
+                    t.record_stream(call.compute)
             if call.done is None:
                 call.compute.wait_stream(call.stream)
         return EventOverlap(call.done, tuple(keep))

@@ -218,3 +218,35 @@ def test_buffer_comm_stream_follows_a_delayed_compute_stream():
         n = int(counts[d])
         np.testing.assert_array_equal(host_bits(recv_x[d])[:n], exp["recv_x"][off[d]:off[d] + n])
     assert buf.check_errors() == 0
+
+
+def test_buffer_comm_pool_outputs_stay_reserved_for_compute_stream_readers():
+    """allocate_on_comm_stream: the outputs come from the comm stream's pool and are read
+    on the compute stream. A compute-stream reader, delayed by a bounded busy kernel, must
+    still see the first call's outputs after the host has dropped them and later calls
+    (waiting only on an older previous_event, not on the compute stream) allocated from
+    the same pool and ran."""
+    import dataclasses
+    inp, _, topk, _ = _inputs()
+    inp2 = workloads.make_workload(dataclasses.replace(W, seed=502), with_hidden=False)
+    topk2 = torch.from_numpy(inp2["topk_idx"]).cuda()
+    buf = Buffer(W.R, W.E, W.H, W.k, W.C)
+    stale = buf.capture()
+    torch.cuda.synchronize()
+    _, _, ntpe, in_rank, ev = buf.get_dispatch_layout(topk, previous_event=stale, async_finish=True,
+                                                      allocate_on_comm_stream=True)
+    ev.current_stream_wait()
+    torch.cuda._sleep(20_000_000)          # the reader below runs late (bounded busy kernel)
+    seen_rank, seen_expert = in_rank.clone(), ntpe.clone()
+    del ntpe, in_rank, ev
+    # The Buffer keeps the latest layout, so the first call's buffers are released by the
+    # second call and may be handed out again to the third.
+    for _ in range(2):
+        out = buf.get_dispatch_layout(topk2, previous_event=stale, async_finish=True,
+                                      allocate_on_comm_stream=True)
+        del out
+    torch.cuda.synchronize()
+    ref = oracle.layout(inp["topk_idx"], W.E, W.C)
+    np.testing.assert_array_equal(seen_rank.cpu().numpy(), ref["is_token_in_rank"])
+    np.testing.assert_array_equal(seen_expert.cpu().numpy(), ref["num_tokens_per_expert"])
+    assert buf.check_errors() == 0
