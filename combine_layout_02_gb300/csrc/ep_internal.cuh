@@ -86,11 +86,17 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
     return m;
 }
 
-// Programmatic dependent launch. Every kernel of the library calls pdl_wait() before
-// its first global-memory access, so a kernel launched early (while the previous kernel
-// of the stream still runs) only overlaps its launch latency, never its memory work.
-// pdl_trigger() lets the next kernel of the stream start launching. Both are no-ops
-// for kernels launched without the programmatic-serialization attribute.
+// Programmatic dependent launch. A kernel launched early (while the previous kernel of
+// the stream still runs) must call pdl_wait() before it reads anything the previous
+// kernel may write and before its first global store, so it overlaps only the previous
+// kernel's tail. Kernels that may follow arbitrary caller work wait before their first
+// global access. The one exception is a kernel that only ever follows a kernel of this
+// library which itself returned from pdl_wait() before its pdl_trigger(): everything
+// ordered before that earlier kernel is then complete, so the later kernel may read
+// the call's inputs before its own wait (the low-latency send kernel does this after the
+// send phase's count kernel). pdl_trigger() lets the next kernel of the stream start
+// launching. Both are no-ops for kernels launched without the
+// programmatic-serialization attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -14,22 +14,28 @@
 // Reading of the receive format: rank d keeps, for each local expert el, R*Nmax
 // slots; source s owns [s*Nmax, (s+1)*Nmax) and fills them in the order of its
 // (token, k) entries: entry (t, j) of source s with expert e takes slot
-//   s*Nmax + #{(t', j') before (t, j) in source s with expert e}.
-// The send kernel computes that count by a block-wide scan of the source's entries in
-// earlier tokens (at most Nmax*k of them; one shared-memory lookup each, in a table from
-// expert to the token's entry), plus the token's own earlier entries with the same
-// expert (a match-any vote), so no block waits on another.
+//   s*Nmax + #{(t', j') before (t, j) in source s with expert e}   (its in-source rank).
 //
 // Packed variant (no gaps between the sources): entry (t, j) of source s takes
 //   sum over s' < s of count[s'][e] + (the same in-source rank),
 // so the per-source counts must exist before any row is placed.
 //
-// Send phase, both layouts: a small kernel with one block per source writes the per-
-// (destination, expert, source) counts (the count signals the receive phase reads) and
-// lets the send kernel start at once; the send kernel loads its row and ranks its
-// entries, then waits for the counts (programmatic dependent launch) before it writes
-// anything. With the receive phase in the same call, R extra blocks of the send kernel
-// turn the signals into recv_expert_count / layout_range.
+// Send phase, both layouts, two kernels:
+//   ll_rank_kernel -- one block per source: the in-source rank of every entry, in entry
+//       order, chunk by chunk (a match-any vote within each warp, a table of per-warp
+//       counts per expert scanned across the warps, a running count per expert across
+//       chunks): linear in the source's T*k entries. It writes the slot array (the final
+//       slot, or the in-source rank for the packed layout) and the per-(destination,
+//       expert, source) counts, the signals the receive phase reads. It waits for
+//       everything earlier before it triggers the send kernel's launch.
+//   ll_send_kernel -- one block per source token: loads its row and its expert ids and
+//       quantises the row while the rank kernel runs, waits for it (programmatic
+//       dependent launch), reads its slots (adding the earlier sources' counts for the
+//       packed layout), then stores the row to every destination slot.
+// With the receive phase in the same call, R extra blocks of the send kernel turn the
+// signals into recv_expert_count / layout_range.
+#include <mutex>
+
 #include "rowops.cuh"
 
 namespace ep {
@@ -38,8 +44,18 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kCombineU = 1;        // units per thread per batch in the LL combine
 constexpr int kSendThreads = 128;   // threads per token block of the send kernel
-constexpr int kSendPre = 8;         // 16-byte row pieces per thread loaded before the scan
-constexpr int kSendScanPre = 8;     // earlier entries per thread loaded up front
+constexpr int kSendPre = 8;         // 16-byte row pieces per thread loaded before the wait
+constexpr int kSendBlocksPerSm = 7; // the decode shape's 1024 token blocks in one wave
+constexpr int kRankThreads = 1024;  // rank kernel: one block per source
+constexpr int kRankWarps = kRankThreads / 32;
+constexpr int kRankSmemMax = 96 * 1024;       // [warps per chunk][E] table + [E] counts
+
+// Warps (of 32 entries each) per chunk of the rank kernel, so that its table and the
+// running counts fit (at least one warp: 64 KB at the largest E).
+inline int rank_chunk_warps(int E) {
+    const int w = kRankSmemMax / (int)(sizeof(int) * E) - 1;
+    return w < 1 ? 1 : (w > kRankWarps ? kRankWarps : w);
+}
 
 __device__ __forceinline__ int ceil_div_dev(int a, int b) { return (a + b - 1) / b; }
 
@@ -58,6 +74,7 @@ struct LLArgs {
     char* out;
     int R, T, H, E, k, E_loc, nmax, use_fp8, write_recv, packed;
     int col_split;                  // combine: blocks per token (column ranges)
+    int cw;                         // rank kernel: warps per chunk
     QuantMode qm;                   // send phase with use_fp8: scale format
     uint32_t* err;
 };
@@ -91,37 +108,78 @@ __device__ __forceinline__ void expert_ranges_warp(const LLArgs& a, int64_t e, i
     if (lane == 0) a.recv_expert_count[e] = t0 + t1;
 }
 
-// Send phase, first kernel: block s counts source s's entries per expert (capped at
-// Nmax, as the send kernel caps them) into send_count[e][s]. It waits for everything
-// earlier, then lets the send kernel launch: that kernel reads only inputs before its
-// own wait.
-__global__ void __launch_bounds__(kThreads) ll_count_kernel(LLArgs a) {
-    extern __shared__ int hist[];   // [E]
-    const int s = blockIdx.x;
+// An expert id as int32: ids in [-1, E) unchanged, anything else -2 (a bad entry).
+__device__ __forceinline__ int ll_id32(int64_t e, int E) { return (e >= -1 && e < E) ? (int)e : -2; }
+
+// Send phase, first kernel: block s ranks source s's entries (see the file header). The
+// entries go through in chunks of cw warps x 32 entries, in entry order: within a warp
+// the rank is the number of earlier lanes with the same expert (match-any vote); the
+// warp's count per expert goes into a [cw][E] table, whose exclusive scan over the warps,
+// started at the expert's running count of the earlier chunks, gives each warp's base.
+__global__ void __launch_bounds__(kRankThreads) ll_rank_kernel(LLArgs a) {
+    extern __shared__ int rsm[];
+    int* wtab = rsm;                  // [cw][E]
+    int* carry = rsm + a.cw * a.E;    // [E] running count per expert
+    const int s = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = a.T * a.k, chunk = a.cw * 32;
+    const bool act = warp < a.cw;
+    const int64_t* tk = a.topk_idx + (int64_t)s * n;
+    int32_t* slot = a.slot + (int64_t)s * n;
+    // Everything earlier in the stream is complete past this wait, so the send kernel may
+    // read the call's inputs as soon as it starts.
     pdl_wait();
     pdl_trigger();
-    for (int i = threadIdx.x; i < a.E; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < a.T * a.k; i += kThreads) {
-        const int64_t e = __ldg(tk + i);
-        if (e >= 0 && e < a.E) atomicAdd(&hist[(int)e], 1);
+    int cur = (act && warp * 32 + lane < n) ? ll_id32(__ldg(tk + warp * 32 + lane), a.E) : -1;
+    for (int e = threadIdx.x; e < a.E; e += kRankThreads) carry[e] = 0;
+    for (int c0 = 0; c0 < n; c0 += chunk) {              // block-uniform trip count
+        const int i = c0 + warp * 32 + lane;
+        const int in = i + chunk;
+        const int nxt = (act && in < n) ? ll_id32(__ldg(tk + in), a.E) : -1;   // next chunk
+        for (int x = threadIdx.x; x < a.cw * a.E; x += kRankThreads) wtab[x] = 0;
+        __syncthreads();
+        const int e = cur;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e >= 0 ? e : -1 - lane);
+        const int rw = __popc(peers & lanemask_lt());
+        if (act && e >= 0 && rw == 0) wtab[warp * a.E + e] = __popc(peers);
+        __syncthreads();
+        for (int ee = threadIdx.x; ee < a.E; ee += kRankThreads) {
+            int v[kRankWarps];
+#pragma unroll
+            for (int w = 0; w < kRankWarps; ++w) v[w] = w < a.cw ? wtab[w * a.E + ee] : 0;
+            int c = carry[ee];
+#pragma unroll
+            for (int w = 0; w < kRankWarps; ++w) {
+                if (w < a.cw) wtab[w * a.E + ee] = c;
+                c += v[w];
+            }
+            carry[ee] = c;
+        }
+        __syncthreads();
+        if (act && i < n) {
+            int32_t pos = -1;
+            if (e == -2) {
+                raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
+            } else if (e >= 0) {
+                const int rank = wtab[warp * a.E + e] + rw;
+                if (rank >= a.nmax) raise_flag(a.err, EP_DEVERR_SLOT_OVERFLOW);
+                else pos = a.packed ? rank : s * a.nmax + rank;
+            }
+            slot[i] = pos;
+        }
+        cur = nxt;
+        __syncthreads();                                 // the table is reused
     }
-    __syncthreads();
-    for (int e = threadIdx.x; e < a.E; e += kThreads)
-        a.send_count[(int64_t)e * a.R + s] = min(hist[e], a.nmax);
+    for (int e = threadIdx.x; e < a.E; e += kRankThreads)
+        a.send_count[(int64_t)e * a.R + s] = min(carry[e], a.nmax);
 }
 
 // Blocks [0, R*T): one per source token. With the receive phase in the same call
 // (write_recv), blocks [R*T, R*T + R): destination d's recv_expert_count and
 // layout_range from the count kernel's signals.
-__global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
+__global__ void __launch_bounds__(kSendThreads, kSendBlocksPerSm) ll_send_kernel(LLArgs a) {
     __shared__ int64_t s_e[EP_MAX_TOPK];
-    __shared__ int s_cnt[EP_MAX_TOPK];
     __shared__ int64_t s_rows[EP_MAX_TOPK];
     __shared__ int s_nv;
-    extern __shared__ int hist[];   // [E]: expert -> one of the token's entries
     const int b = blockIdx.x;
     const int64_t slots = (int64_t)a.R * a.nmax;
 
@@ -137,8 +195,8 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
     const int s = b / a.T, t = b - s * a.T;
     const int64_t tok = (int64_t)s * a.T + t;
     const char* src = a.x + tok * (int64_t)a.H * 2;
-    // The token's row does not depend on the slot ranks: load its first batch now, so the
-    // load overlaps the rank scan below.
+    // The token's row and expert ids are inputs of the call: they are loaded while the
+    // rank kernel runs.
     const int qunits = a.H >> 4;                 // fp8: 16 channels per unit
     const int cunits = a.H >> 3;                 // bf16 copy: 8 channels per unit
     uint4 pre[kSendPre];
@@ -153,46 +211,19 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
             if (u < cunits) pre[i] = ld_stream_v4(src + (int64_t)u * 16);
         }
     }
-    // The source's entries in earlier tokens (for the slot ranks) do not depend on this
-    // token either: each thread loads its first kScanPre of them now, with the row and
-    // the token's own ids, so all three share one memory round trip.
-    const int64_t* tk = a.topk_idx + (int64_t)s * a.T * a.k;
-    const int lim = t * a.k;
-    int64_t pre_e[kSendScanPre];
+    if (threadIdx.x < a.k) s_e[threadIdx.x] = a.topk_idx[tok * a.k + threadIdx.x];
+    // The quantised units do not depend on where they go: quantise them while the rank
+    // kernel still runs (block-uniform branch: every lane takes part in the shuffles).
+    uint4 qv[kSendPre / 2];
+    float qs[kSendPre / 2];
+    uint32_t qb[kSendPre / 2];
+    if (a.use_fp8) {
 #pragma unroll
-    for (int q = 0; q < kSendScanPre; ++q) {
-        const int i = threadIdx.x + q * kSendThreads;
-        pre_e[q] = i < lim ? __ldg(tk + i) : -1;
-    }
-    // hist[e] (the block's E ints, not cleared): one of this token's entries with
-    // expert e. A value left by another block is never used for an expert outside this
-    // token: a lookup counts only if the entry it names has that very expert.
-    if (threadIdx.x < a.k) {
-        const int64_t e = a.topk_idx[tok * a.k + threadIdx.x];
-        s_e[threadIdx.x] = e;
-        s_cnt[threadIdx.x] = 0;
-        if (e >= 0 && e < a.E) hist[(int)e] = threadIdx.x;
+        for (int i = 0; i < kSendPre / 2; ++i) qv[i] = quant_unit(pre[2 * i], pre[2 * i + 1], a.qm, qs[i], qb[i]);
     }
     __syncthreads();
-
-    // Count of the source's entries in earlier tokens with each of this token's experts,
-    // booked on the entry the table names (one shared-memory lookup per entry).
-#pragma unroll
-    for (int q = 0; q < kSendScanPre; ++q) {
-        const int64_t e = pre_e[q];
-        if (e < 0 || e >= a.E) continue;
-        const int j = hist[(int)e];
-        if ((unsigned)j < (unsigned)a.k && s_e[j] == e) atomicAdd(&s_cnt[j], 1);
-    }
-    for (int i = threadIdx.x + kSendScanPre * kSendThreads; i < lim; i += kSendThreads) {
-        const int64_t e = __ldg(tk + i);
-        if (e < 0 || e >= a.E) continue;
-        const int j = hist[(int)e];
-        if ((unsigned)j < (unsigned)a.k && s_e[j] == e) atomicAdd(&s_cnt[j], 1);
-    }
-    __syncthreads();
-    // Nothing before this wait wrote: the count kernel's signals (the packed layout's
-    // earlier-source counts) are complete after it.
+    // Nothing before this wait wrote: the rank kernel's slots and counts are complete
+    // after it.
     pdl_wait();
 
     // Warp 0 (k <= 32 lanes) places the entries and compacts the valid rows in entry
@@ -200,32 +231,20 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
     if (threadIdx.x < 32) {
         const int j = threadIdx.x;
         int64_t row = -1;
-        // Rank = count in earlier tokens + this token's earlier entries with the same
-        // expert (lanes >= k hold distinct values that match nothing).
-        const int64_t ej = j < a.k ? s_e[j] : -2 - (int64_t)j;
-        const unsigned same = __match_any_sync(0xFFFFFFFFu, (unsigned long long)ej);
         if (j < a.k) {
-            const int64_t e = ej;
-            int32_t pos = -1;
-            if (e >= a.E || e < -1) {
-                raise_flag(a.err, EP_DEVERR_BAD_EXPERT);
-            } else if (e >= 0) {
-                const int rank = s_cnt[hist[(int)e]] + __popc(same & lanemask_lt());
-                if (rank >= a.nmax) {
-                    raise_flag(a.err, EP_DEVERR_SLOT_OVERFLOW);
-                } else {
-                    const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
-                    int start = s * a.nmax;
-                    if (a.packed) {
-                        start = 0;
-                        for (int src = 0; src < s; ++src) start += a.send_count[e * a.R + src];
-                    }
-                    pos = start + rank;
-                    row = ((int64_t)d * a.E_loc + el) * slots + pos;
-                    a.src_info[row] = t;
+            // The rank kernel flagged bad ids and overflows and gave them slot -1.
+            const int32_t got = a.slot[tok * a.k + j];
+            if (got >= 0) {
+                const int64_t e = s_e[j];
+                const int d = (int)(e / a.E_loc), el = (int)(e - (int64_t)d * a.E_loc);
+                int32_t pos = got;
+                if (a.packed) {          // got = in-source rank; add the earlier sources' counts
+                    for (int src = 0; src < s; ++src) pos += a.send_count[e * a.R + src];
+                    a.slot[tok * a.k + j] = pos;
                 }
+                row = ((int64_t)d * a.E_loc + el) * slots + pos;
+                a.src_info[row] = t;
             }
-            a.slot[tok * a.k + j] = pos;
         }
         const unsigned bal = __ballot_sync(0xFFFFFFFFu, row >= 0);
         if (row >= 0) s_rows[__popc(bal & lanemask_lt())] = row;
@@ -237,13 +256,10 @@ __global__ void __launch_bounds__(kSendThreads) ll_send_kernel(LLArgs a) {
     if (a.use_fp8) {
         uint8_t* q_base = reinterpret_cast<uint8_t*>(a.recv_x);
 #pragma unroll
-        for (int i = 0; i < kSendPre / 2; ++i) { // the prefetched units (all lanes shuffle)
+        for (int i = 0; i < kSendPre / 2; ++i) { // the units quantised before the wait
             const int u = threadIdx.x + i * kSendThreads;
-            float scale;
-            uint32_t sbyte;
-            const uint4 q = quant_unit(pre[2 * i], pre[2 * i + 1], a.qm, scale, sbyte);
             if (u < qunits)
-                store_quant_unit(q_base, a.recv_x_scales, s_rows, nv, a.H, u, q, scale, sbyte, a.qm.mode);
+                store_quant_unit(q_base, a.recv_x_scales, s_rows, nv, a.H, u, qv[i], qs[i], qb[i], a.qm.mode);
         }
         scatter_quant_row<1>(src, q_base, a.recv_x_scales, s_rows, nv, a.H, a.qm, threadIdx.x,
                              kSendThreads, kSendPre / 2 * kSendThreads);
@@ -312,6 +328,23 @@ __global__ void __launch_bounds__(kThreads) ll_combine_kernel(LLArgs a) {
     pdl_trigger();
 }
 
+// Lets the rank kernel use up to kRankSmemMax of dynamic shared memory (once per device).
+cudaError_t rank_kernel_smem_attribute() {
+    static std::mutex mu;
+    static bool done[128];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(ll_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRankSmemMax);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
 ep_status ll_common_checks(const ep_shape* sh, const ep_launch* launch) {
     ep_status st = check_shape(sh);
     if (st != EP_OK) return st;
@@ -319,6 +352,9 @@ ep_status ll_common_checks(const ep_shape* sh, const ep_launch* launch) {
     if (sh->num_max_dispatch_tokens_per_rank < 1) return EP_ERR_INVALID_ARG;
     if (sh->num_tokens > sh->num_max_dispatch_tokens_per_rank) return EP_ERR_INVALID_ARG;
     if ((int64_t)sh->num_ranks * sh->num_max_dispatch_tokens_per_rank > (int64_t)1 << 30)
+        return EP_ERR_UNSUPPORTED;
+    // Entry counts of one source (T*k) and of all sources (R*T*k) are int32 in the kernels.
+    if ((int64_t)sh->num_ranks * sh->num_tokens * sh->num_topk > (int64_t)INT32_MAX)
         return EP_ERR_UNSUPPORTED;
     return EP_OK;
 }
@@ -381,14 +417,16 @@ ep_status ep_ll_dispatch(const ep_shape* sh, const void* x, const int64_t* topk_
 
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (phase & EP_PHASE_SEND) {
-        cudaError_t e = launch_pdl(ll_count_kernel, dim3((unsigned)a.R), dim3(kThreads),
-                                   sizeof(int) * (size_t)a.E, launch->stream, a);
+        a.cw = rank_chunk_warps(a.E);
+        cudaError_t e = rank_kernel_smem_attribute();
+        if (e == cudaSuccess)
+            e = launch_pdl(ll_rank_kernel, dim3((unsigned)a.R), dim3(kRankThreads),
+                                   sizeof(int) * (size_t)(a.cw + 1) * a.E, launch->stream, a);
         if (e == cudaSuccess) {
             // Token blocks, plus one receive-output block per destination with BOTH.
             const unsigned blocks = (unsigned)(a.R * a.T + (a.write_recv ? a.R : 0));
             if (blocks > 0)
-                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kSendThreads), sizeof(int) * (size_t)a.E,
-                               launch->stream, a);
+                e = launch_pdl(ll_send_kernel, dim3(blocks), dim3(kSendThreads), 0, launch->stream, a);
         }
         if (e != cudaSuccess) return cuda_fail(e);
     }

@@ -151,6 +151,15 @@ def test_invalid_arguments_rejected_on_host(ep):
     st = L.ep_ll_combine(ctypes.byref(sh_ll2), 0x3000, 0x4000, 0x5000, ctypes.byref(buf),
                          8, 0x6000, ctypes.byref(launch))
     assert st == ep.EP_ERR_INVALID_ARG
+    # low-latency: a source's entry count T*k beyond int32 (R*T and R*Nmax within limits)
+    huge = ep.make_shape(1, 1 << 28, 128, 8, 8, nmax=1 << 28)
+    for phase in (ep.EP_PHASE_SEND, ep.EP_PHASE_RECV, ep.EP_PHASE_BOTH):
+        st = L.ep_ll_dispatch(ctypes.byref(huge), 0x7000, 0x8000, 0, phase, ctypes.byref(buf),
+                              ctypes.byref(launch))
+        assert st == ep.EP_ERR_UNSUPPORTED, phase
+    st = L.ep_ll_combine(ctypes.byref(huge), 0x3000, 0x4000, 0x5000, ctypes.byref(buf),
+                         ep.EP_PHASE_RECV, 0x6000, ctypes.byref(launch))
+    assert st == ep.EP_ERR_UNSUPPORTED
     # unsupported shape
     big = ep.make_shape(65, 4, 128, 65, 1)
     st = L.ep_dispatch(ctypes.byref(big), 0x3000, ep.EP_BF16, None, ep.EP_BF16, None, None,
