@@ -11,6 +11,8 @@
 //
 // The array lives in device memory of every GPU that loads the library, for the life
 // of the process, whether or not this entry point is ever called.
+#include <cuda.h>   // driver types only (the driver functions are looked up at run time)
+
 #include <mutex>
 
 #include "ep_internal.cuh"
@@ -20,8 +22,49 @@
 static __device__ __align__(256) unsigned char g_layout_scratch[EP_LAYOUT_STATIC_SCRATCH_BYTES];
 
 namespace {
+
+// The array's device address belongs to the module loaded into one CUDA context. After
+// cudaDeviceReset (or any new primary context) the module is loaded again, possibly at
+// another address, so the cached address is keyed by the context's unique id.
+struct ScratchAddr {
+    unsigned long long ctx_id;
+    void* addr;
+};
+
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[128] = {nullptr};   // device address of g_layout_scratch, per device
+ScratchAddr g_scratch_addr[128] = {};        // per device ordinal
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// Looks up the two driver functions once (no link-time dependency on libcuda).
+bool driver_functions() {
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    return g_ctx_get_current != nullptr && g_ctx_get_id != nullptr;
+}
+
+// Id of the current context (0 if there is none yet).
+bool current_ctx_id(unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return false;
+    *id = 0;
+    if (ctx == nullptr) return true;
+    return g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" ep_status ep_get_layout_static_scratch(const ep_shape* shape, const int64_t* topk_idx,
@@ -36,18 +79,25 @@ extern "C" ep_status ep_get_layout_static_scratch(const ep_shape* shape, const i
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return ep::cuda_fail(e);
     if (dev < 0 || dev >= 128) return EP_ERR_UNSUPPORTED;
+    if (!driver_functions()) return EP_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     {
-        // One-time set-up per device, with that device current: resolve the array's
-        // device address.
+        // Set-up once per context, with the device current: resolve the array's device
+        // address. A context seen for the first time (the first call, or the first after
+        // a device reset) repeats the lookup.
         std::lock_guard<std::mutex> lock(g_scratch_mutex);
-        if (g_scratch_addr[dev] == nullptr) {
+        unsigned long long id = 0;
+        if (!current_ctx_id(&id)) return EP_ERR_UNSUPPORTED;
+        ScratchAddr& c = g_scratch_addr[dev];
+        if (id == 0 || c.addr == nullptr || c.ctx_id != id) {
             void* p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_layout_scratch);
+            e = cudaGetSymbolAddress(&p, g_layout_scratch);   // creates the context if needed
             if (e != cudaSuccess) return ep::cuda_fail(e);
-            g_scratch_addr[dev] = p;
+            if (!current_ctx_id(&id) || id == 0) return EP_ERR_UNSUPPORTED;
+            c.ctx_id = id;
+            c.addr = p;
         }
-        scratch = g_scratch_addr[dev];
+        scratch = c.addr;
     }
     // The layout kernels overwrite every scratch word they later read, so the contents
     // left by an earlier call need no clearing.

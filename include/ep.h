@@ -280,8 +280,11 @@ EP_API ep_status ep_get_layout(const ep_shape* shape, const int64_t* topk_idx, e
  *     inside libep.so; every GPU that loads the library holds it until the process
  *     exits. Shapes whose ep_layout_workspace_size exceeds it return
  *     EP_ERR_UNSUPPORTED before anything is enqueued (R=8, C=12, E=256 needs ~97 KiB).
- *   - The first call on a device (with that device current) looks up the array's
- *     device address; make that first call before any stream capture.
+ *   - The first call in a CUDA context (the first on a device, with that device
+ *     current, and again the first after cudaDeviceReset, when the library's device
+ *     code is loaded anew) looks up the array's device address; make that first call
+ *     before any stream capture. A device reset makes an address cached earlier
+ *     invalid, which is why the cache is keyed by the context.
  *   - The call itself allocates nothing and frees nothing.
  *   - All calls on a device share the one array. Calls whose kernels may overlap on
  *     the GPU (different streams without ordering between them) race on it and give
