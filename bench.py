@@ -7,22 +7,31 @@ softmax weights, 12 channels, receive regions sized for the worst case (no host 
 
 Prints one JSON line. `value` is the effective HBM bandwidth of the whole step
 (algorithmic bytes of layout + dispatch + combine / device time per step, inputs
-resident in HBM, inputs larger than L2), timed over K steps with CUDA events only around
-the region, so the kernels chain through programmatic dependent launch as in use.
-`dispatch_gbs`, `combine_gbs`, `layout_dispatch_us` and `roofline` come from a second
-timed pass of the same K steps with CUDA events on the launching stream around every
-phase. `layout_dispatch_synced_us` is the exact-size variant: layout, a host wait for the
-received counts, then the dispatch into regions of exactly those sizes. `e2e` is the same metric through the same C-ABI
-calls with host buffers: pinned host -> device copy of x / topk_idx / topk_weights and
-a device -> host copy of the combined output inside every timed step.
+resident in HBM, inputs larger than L2), timed with CUDA events only around each region
+of K steps, so the kernels chain through programmatic dependent launch as in use. Every
+timed pass repeats its K steps until half a second of wall time has passed, so the
+nvidia-smi clock sampler sees the whole window under load; figures are means over all
+repeats (`repeats`, `timed_steps`). `dispatch_gbs`, `combine_gbs`, `layout_dispatch_us`
+and `roofline` come from a second timed pass of the same steps with CUDA events on the
+launching stream around every phase. `layout_dispatch_synced_us` is the exact-size
+variant: layout, a host wait for the received counts, then the dispatch into regions of
+exactly those sizes. `e2e` is the same metric through the same C-ABI calls with host
+buffers: pinned host -> device copy of x / topk_idx / topk_weights and a device -> host
+copy of the combined output inside every timed step.
 
---workload picks another step (group_limited, zipf_reuse, ll_decode, ll_decode_packed,
-dsv3_expert_major, dsv3_backward; see WORKLOAD_TEXT); --fp8-scale picks the scale format of
-the e4m3 sends. The roofline's traffic comes from the committed ncu counters only when
-they were taken on the same workload and kernel sources.
+The same line carries, under `workloads`, the other workloads of the benchmark, each
+timed the same way with its own roofline and clock record: group_limited (fused e4m3
+dispatch + combine), zipf_reuse (dispatch and combine with a cached handle) and
+ll_decode (low-latency send, receive hook and combine, L2 flushed before every step).
+--workload picks another step as the headline instead (group_limited, zipf_reuse,
+ll_decode, ll_decode_packed, dsv3_expert_major, dsv3_backward; see WORKLOAD_TEXT);
+--fp8-scale picks the scale format of the e4m3 sends. The roofline's traffic comes from
+the committed ncu counters only when they were taken on the same workload and kernel
+sources.
 
 --impl reference times the CPU oracle (test infrastructure; single-threaded C) on a
-bounded token sample of the same workload and prints the same metric.
+bounded token sample of the same workload and prints the same metric with the same
+config.
 
 Multi-GPU: the path does not shard (virtual ranks live in one GPU's memory), so
 `--gpus N` under torchrun runs N independent replicas; the barrier and max-over-ranks
@@ -76,7 +85,13 @@ def measured_peaks():
 
 KERNEL_SOURCES = {
     "dispatch_tma_kernel": ("dispatch.cu", "rowops.cuh", "ep_internal.cuh"),
+    "dispatch_kernel<quant>": ("dispatch.cu", "rowops.cuh", "ep_internal.cuh"),
     "combine_kernel": ("combine.cu", "rowops.cuh", "ep_internal.cuh"),
+    "ll_send_kernel": ("ll.cu", "rowops.cuh", "ep_internal.cuh"),
+    "ll_combine_kernel": ("ll.cu", "rowops.cuh", "ep_internal.cuh"),
+    "dispatch_em_tma_kernel": ("expert_major.cu", "rowops.cuh", "ep_internal.cuh"),
+    "combine_em_kernel": ("expert_major.cu", "rowops.cuh", "ep_internal.cuh"),
+    "layout_cluster_kernel": ("layout.cu", "ep_internal.cuh"),
 }
 
 
@@ -91,21 +106,18 @@ def source_digest(files):
 
 
 def traffic_from_profiles(kernel: str, workload: str = "dsv3"):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken
-    on the current kernel sources and on `workload` (else None)."""
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu counters,
+    if they were taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     with open(path) as f:
-        entries = json.load(f)
-    e = entries.get(kernel)
-    if not e or kernel not in KERNEL_SOURCES:
-        return None
-    if e.get("source_sha256") != source_digest(KERNEL_SOURCES[kernel]):
-        return None
-    if e.get("workload", "dsv3") != workload:
-        return None
-    return e.get("dram_bytes_per_launch")
+        entries = json.load(f).get("entries", [])
+    digest = source_digest(KERNEL_SOURCES[kernel])
+    for e in entries:
+        if e.get("kernel") == kernel and e.get("workload") == workload and e.get("source_sha256") == digest:
+            return e.get("dram_bytes_per_launch")
+    return None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -366,6 +378,7 @@ WORKLOAD_TEXT = {
 }
 BASE_WORKLOAD = {"dsv3_expert_major": "dsv3", "ll_decode_packed": "ll_decode", "dsv3_backward": "dsv3"}
 FP8_SCALE = {"fp32": 0, "pow2": 1, "ue8m0": 2, "tensor": 3}
+DSV3_L2 = "inputs larger than L2; no flush"
 
 
 def workload_config(name: str):
@@ -464,6 +477,11 @@ def make_plan(args, ep, dev, stream, launch):
 
         if not reuse:
             plan["layout_dispatch_synced"] = layout_dispatch_synced
+            # The layout runs as one cluster launch or as two kernels, by shape.
+            n0 = ep.ep_kernel_launch_count()
+            layout()
+            plan["layout_kernels"] = ("layout_cluster_kernel" if ep.ep_kernel_launch_count() - n0 == 1
+                                      else "layout_count+layout_prefix")
         dname = "dispatch_fp8" if fp8 else "dispatch"
         # The plan owns every buffer whose raw pointers the calls use.
         plan["keep"] = (lb, rb, y, out, xs)
@@ -531,6 +549,7 @@ def make_plan(args, ep, dev, stream, launch):
         layout_s, handle = lb.layout(), lb.handle()
         plan["keep"] = (lb, recv_x, recv_w, recv_src, out)
         plan["out"] = out
+        plan["layout_kernels"] = "layout_count+layout_prefix+layout_expert_rows"
         plan["phases"] = [
             ("layout", lambda: ep.ep_get_layout(sh, topk, layout_s, handle, lb.workspace, launch)),
             ("dispatch_em", lambda: ep.ep_dispatch_expert_major(sh, x, ep.EP_BF16, topk, wts, handle,
@@ -644,16 +663,24 @@ def run_graph(args, world, dev, launch, step, flush_buf, total_bytes):
             "unit": "GB/s"}
 
 
-def run_ours(args, rank, world):
-    import torch
-    import combine_layout_02_gb300 as ep
+MIN_WINDOW_S = 0.5       # each timed pass repeats its K steps until this much wall time passed
+MAX_REPEATS = 2000
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    ep.lib()                                              # fails loudly without libep.so
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream()
-    launch = ep.make_launch(stream, error_flags=err)
+
+def config_dict(name, w, units, world, l2):
+    """The `config` object of a bench line (shared by the GPU and the reference arm)."""
+    key = "valid_entries" if name in ("ll_decode", "ll_decode_packed", "dsv3_expert_major") else "recv_rows"
+    return {"workload": f"{name}: " + WORKLOAD_TEXT[name].format(T=w.T),
+            "R": w.R, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "C": w.C, key: units,
+            "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)", "l2": l2}
+
+
+def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
+    """Times one workload's step (args.workload) and returns (result dict, inputs, plan
+    extras). Every timed pass repeats its K steps until MIN_WINDOW_S of wall time have
+    passed, so the clock sampler sees the GPU under load for the whole window; the
+    figures are means over all repeats."""
+    import torch
     plan = make_plan(args, ep, dev, stream, launch)
     phases = plan["phases"]
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if plan["flush"] else None
@@ -674,70 +701,77 @@ def run_ours(args, rank, world):
     nbytes, units = plan["nbytes"]()
     total_bytes = sum(nbytes.values())
 
-    def timed_region(sampler, per_phase, flush=True):
-        """K steps between a barrier and a synchronisation on each side. per_phase=False
-        (the headline pass): events only around the whole region (around each step when
-        L2 is flushed between steps, so the flush stays outside), so consecutive kernels
-        overlap through programmatic dependent launch as they do in use. per_phase=True
-        (the breakdown pass): an event before and after every phase."""
+    def timed_window(sampler, per_phase, flush=True):
+        """Repeats of K steps between a barrier and a synchronisation on each side, until
+        MIN_WINDOW_S have passed. per_phase=False (the headline pass): events only around
+        each K-step region (around each step when L2 is flushed between steps, so the flush
+        stays outside), so consecutive kernels overlap through programmatic dependent
+        launch as they do in use. per_phase=True (the breakdown pass): an event before and
+        after every phase. Returns (ms per step, per-phase ms lists, launches, clocks,
+        repeats)."""
         n = args.steps
         fbuf = flush_buf if flush else None
-        if per_phase:
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(n)]
-        elif fbuf is not None:
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        else:
-            evs = None
         barrier(world)
         torch.cuda.synchronize()
         n0 = ep.ep_kernel_launch_count()
         if sampler:
             sampler.start()
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(n):
-            if fbuf is not None:
-                fbuf.zero_()
+        t0 = time.perf_counter()
+        total_ms, reps = 0.0, 0
+        per = {name: [] for name, _ in phases} if per_phase else None
+        while True:
             if per_phase:
-                step(evs[i])
-            elif evs is not None:
-                evs[i][0].record(stream)
-                step()
-                evs[i][1].record(stream)
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(n)]
+            elif fbuf is not None:
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
             else:
-                step()
-        t_end.record(stream)
-        torch.cuda.synchronize()
+                evs = None
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_start.record(stream)
+            for i in range(n):
+                if fbuf is not None:
+                    fbuf.zero_()
+                if per_phase:
+                    step(evs[i])
+                elif evs is not None:
+                    evs[i][0].record(stream)
+                    step()
+                    evs[i][1].record(stream)
+                else:
+                    step()
+            t_end.record(stream)
+            torch.cuda.synchronize()
+            reps += 1
+            if per_phase:
+                for i, (name, _) in enumerate(phases):
+                    per[name].extend(e[i].elapsed_time(e[i + 1]) for e in evs)
+            if evs is not None:
+                total_ms += sum(e[0].elapsed_time(e[-1]) for e in evs)
+            else:
+                total_ms += t_start.elapsed_time(t_end)
+            if time.perf_counter() - t0 >= args.min_window_s or reps >= MAX_REPEATS:
+                break
         clocks = sampler.stop() if sampler else None
         barrier(world)
         launches = ep.ep_kernel_launch_count() - n0
-        per = ({name: [e[i].elapsed_time(e[i + 1]) for e in evs] for i, (name, _) in enumerate(phases)}
-               if per_phase else None)
-        if evs is not None:
-            total_ms = sum(e[0].elapsed_time(e[-1]) for e in evs)
-        else:
-            total_ms = t_start.elapsed_time(t_end)
-        return total_ms, per, launches, clocks
+        return total_ms / (n * reps), per, launches, clocks, reps
 
-    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    gpu_id = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
     remeasured = False
-    total_ms, _, launches, clocks = timed_region(ClockSampler(gpu_id), per_phase=False)
+    ms_step, _, launches, clocks, reps = timed_window(ClockSampler(gpu_id), per_phase=False)
     if clocks and any(r in clocks["reasons"] for r in BAD_REASONS):
         remeasured = True
-        total_ms, _, launches, clocks = timed_region(ClockSampler(gpu_id), per_phase=False)
+        ms_step, _, launches, clocks, reps = timed_window(ClockSampler(gpu_id), per_phase=False)
     # Per-phase breakdown (and the roofline's per-kernel durations): a second timed pass of
-    # the same K steps with an event around every phase.
-    phase_ms, per, _, phase_clocks = timed_region(ClockSampler(gpu_id), per_phase=True)
+    # the same steps with an event around every phase.
+    phase_ms, per, _, phase_clocks, phase_reps = timed_window(ClockSampler(gpu_id), per_phase=True)
     warm = None
     if flush_buf is not None:
         # Small working sets may stay in L2 between steps in use: the same steps unflushed.
-        warm_ms, _, _, _ = timed_region(None, per_phase=False, flush=False)
-        warm_ms = reduce_max(warm_ms / args.steps, world, dev)
-        warm = {"ms_per_step": round(warm_ms, 4), "note": "no L2 flush between steps"}
+        warm_ms, _, _, _, _ = timed_window(None, per_phase=False, flush=False)
+        warm = {"ms_per_step": round(reduce_max(warm_ms, world, dev), 4), "note": "no L2 flush between steps"}
 
-    ms_step = reduce_max(total_ms / args.steps, world, dev)
+    ms_step = reduce_max(ms_step, world, dev)
     flags = int(err.item())
     if flags != 0:
         raise RuntimeError(f"device error flags set: {flags}")
@@ -752,35 +786,19 @@ def run_ours(args, rank, world):
         if int(err.item()) != 0:
             raise RuntimeError(f"device error flags set: {int(err.item())}")
 
-    e2e = None
-    if args.workload == "dsv3" and not args.no_e2e:
-        e2e = run_e2e(world, dev, plan, ep, err, total_bytes, max(4, min(args.steps, 20)),
-                      args.e2e_copy_streams)
-
     peak, peak_kind = measured_peaks()
     w = plan["w"]
-    mean_ms = {name: statistics.mean(v) for name, v in per.items()}
+    mean_ms = {name: reduce_max(statistics.mean(v), world, dev) for name, v in per.items()}
     gbs = {name: nbytes[name] / (mean_ms[name] * 1e6) for name in mean_ms}
     dom = max(mean_ms, key=lambda n: mean_ms[n])
-    value = world * total_bytes / (ms_step * 1e6)
+    kernels = dict(PHASE_KERNEL)
+    if "layout" in phases_names(phases):
+        kernels["layout"] = plan.get("layout_kernels", kernels["layout"])
     result = {
-        "metric": METRIC,
-        "value": round(value, 1),
+        "value": round(world * total_bytes / (ms_step * 1e6), 1),
         "unit": "GB/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": f"{args.workload}: " + WORKLOAD_TEXT[args.workload].format(T=w.T),
-                   "R": w.R, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "C": w.C,
-                   "valid_entries" if args.workload in ("ll_decode", "ll_decode_packed", "dsv3_expert_major") else "recv_rows": units,
-                   "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)",
-                   "l2": plan["l2"]},
+        "config": config_dict(args.workload, w, units, world, plan["l2"]),
     }
     if args.workload in ("group_limited", "ll_decode", "ll_decode_packed"):
         result["config"]["fp8_scale"] = args.fp8_scale
@@ -794,26 +812,95 @@ def run_ours(args, rank, world):
         dname = next(n for n in mean_ms if n.startswith("dispatch"))
         result["layout_dispatch_us"] = round((mean_ms["layout"] + mean_ms[dname]) * 1e3, 2)
     result["bytes_per_step"] = nbytes
-    result["roofline"] = {"bound": "hbm", "kernel": PHASE_KERNEL[dom], "achieved": round(gbs[dom], 1),
+    result["roofline"] = {"bound": "hbm", "kernel": kernels[dom], "achieved": round(gbs[dom], 1),
                           "peak": peak, "unit": "GB/s", "frac": round(gbs[dom] / peak, 4),
-                          "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                          "traffic": traffic_from_profiles(PHASE_KERNEL[dom], args.workload),
+                          "peak_source": f"{peak_kind} hbm_gbs (copy), of {peak_kind}",
+                          "traffic": traffic_from_profiles(kernels[dom], args.workload),
                           "algorithmic_bytes_per_launch": nbytes[dom]}
-    result["e2e"] = e2e
     result["layout_dispatch_synced_us"] = synced
     if warm is not None:
         warm["value"] = round(world * total_bytes / (warm["ms_per_step"] * 1e6), 1)
         result["warm"] = warm
     result["graph"] = graph
-    result["timing"] = ("value / ms_per_step: K steps with events only around the region (around "
-                        "each step when L2 is flushed); *_us, *_gbs and roofline: a second pass of K "
-                        "steps with an event around every phase (its step: "
-                        f"{phase_ms / args.steps:.4f} ms)")
+    result["timing"] = (f"value / ms_per_step: {args.steps} steps with events only around the region "
+                        "(around each step when L2 is flushed), repeated until "
+                        f"{args.min_window_s} s of wall time had passed ({reps} repeats, "
+                        f"{reps * args.steps} steps; the mean over all of them); *_us, *_gbs and "
+                        "roofline: a second pass with an event around every phase "
+                        f"({phase_reps} repeats; its step: {phase_ms:.4f} ms)")
+    result["repeats"] = reps
+    result["timed_steps"] = reps * args.steps
     result["gpu_launches"] = launches
+    result["gpu_launches_per_step"] = round(launches / (reps * args.steps), 3)
     result["clocks"] = clocks
     result["phase_pass_clocks"] = phase_clocks
     result["clocks_remeasured"] = remeasured
-    return result, plan["inp"]
+    return result, plan["inp"], {"plan": plan, "total_bytes": total_bytes}
+
+
+def phases_names(phases):
+    return [name for name, _ in phases]
+
+
+# The extra workloads the default (dsv3) line also measures, each in its own object.
+EXTRA_WORKLOADS = ("group_limited", "zipf_reuse", "ll_decode")
+EXTRA_KEYS = ("value", "unit", "ms_per_step", "config", "layout_us", "dispatch_us", "dispatch_gbs",
+              "dispatch_frac_of_peak", "combine_us", "combine_gbs", "combine_frac_of_peak",
+              "layout_dispatch_us", "ll_send_us", "ll_send_gbs", "ll_send_frac_of_peak", "ll_recv_us",
+              "ll_combine_us", "ll_combine_gbs", "ll_combine_frac_of_peak", "bytes_per_step",
+              "roofline", "warm", "graph", "repeats", "timed_steps", "gpu_launches", "clocks",
+              "phase_pass_clocks", "clocks_remeasured", "layout_dispatch_synced_us")
+
+
+def run_ours(args, rank, world):
+    import copy
+    import torch
+    import combine_layout_02_gb300 as ep
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    ep.lib()                                              # fails loudly without libep.so
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    launch = ep.make_launch(stream, error_flags=err)
+    gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    gpu_id = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
+
+    res, inp, extra = measure_workload(args, world, dev, ep, err, stream, launch, gpu_id)
+    e2e = None
+    if args.workload == "dsv3" and not args.no_e2e:
+        e2e = run_e2e(world, dev, extra["plan"], ep, err, extra["total_bytes"],
+                      max(4, min(args.steps, 20)), args.e2e_copy_streams)
+    del extra
+    torch.cuda.empty_cache()
+    result = {
+        "metric": METRIC,
+        "value": res.pop("value"),
+        "unit": res.pop("unit"),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": res.pop("ms_per_step"),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": res.pop("config"),
+    }
+    result.update(res)
+    result["e2e"] = e2e
+    if args.workload == "dsv3" and not args.no_extra:
+        # The other workloads of the same benchmark, each with its own roofline and clocks.
+        result["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            sub_args = copy.copy(args)
+            sub_args.workload, sub_args.fp8_scale, sub_args.tokens, sub_args.nmax = name, "fp32", 0, 0
+            sub, _, extra = measure_workload(sub_args, world, dev, ep, err, stream, launch, gpu_id)
+            del extra
+            torch.cuda.empty_cache()
+            result["workloads"][name] = {k: sub[k] for k in EXTRA_KEYS if k in sub}
+    return result, inp
 
 
 # ----------------------------------------------------------------------------- oracle
@@ -859,14 +946,16 @@ def run_reference(args, rank, world):
         return None
     inp = workloads.make_workload(WORKLOAD)
     gbs, desc, sec = oracle_sample(inp, args.steps, budget_s=float(os.environ.get("EP_ORACLE_BUDGET_S", 90)))
+    import oracle
+    N = int(oracle.layout(inp["topk_idx"], WORKLOAD.E, WORKLOAD.C)["rank_prefix_matrix"][-1].sum())
     return {
         "impl": "reference",
         "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "dsv3 (token sample, see cpu_baseline.sample)", "R": WORKLOAD.R,
-                   "T": WORKLOAD.T, "H": WORKLOAD.H, "E": WORKLOAD.E, "k": WORKLOAD.k, "C": WORKLOAD.C},
+        # the GPU arm's config of the same workload (the timed sample is in cpu_baseline)
+        "config": config_dict("dsv3", WORKLOAD, N, world, DSV3_L2),
         "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -884,6 +973,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay measurement")
+    ap.add_argument("--min-window-s", type=float, default=MIN_WINDOW_S,
+                    help="each timed pass repeats its K steps until this much wall time has "
+                         "passed (0: one pass of K steps, for profiler captures)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="dsv3 only: skip the group_limited / zipf_reuse / ll_decode objects")
     ap.add_argument("--e2e-copy-streams", type=int, default=1,
                     help="streams per copy direction in the pipelined end-to-end measurement")
     ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default="dsv3",

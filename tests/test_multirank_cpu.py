@@ -73,20 +73,25 @@ def test_every_bench_workload_resolves():
 
 
 def test_roofline_traffic_only_for_its_own_workload_and_sources():
-    """The committed DRAM counters are reported only for the workload and the kernel
-    sources they were taken on; any other workload reads as null."""
+    """The committed DRAM counters are reported only for the (kernel, workload) pair and
+    the kernel sources they were taken on; any other workload reads as null."""
     sys.path.insert(0, ROOT)
     import json
     import bench
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-        entries = json.load(f)
-    for kernel in bench.KERNEL_SOURCES:
-        e = entries[kernel]
-        got = bench.traffic_from_profiles(kernel, e.get("workload", "dsv3"))
+        entries = json.load(f)["entries"]
+    assert entries
+    for e in entries:
+        kernel, workload = e["kernel"], e["workload"]
+        assert kernel in bench.KERNEL_SOURCES and workload in bench.WORKLOAD_TEXT
+        got = bench.traffic_from_profiles(kernel, workload)
         current = e["source_sha256"] == bench.source_digest(bench.KERNEL_SOURCES[kernel])
         assert got == (e["dram_bytes_per_launch"] if current else None)
-        assert bench.traffic_from_profiles(kernel, "zipf_reuse") is None
-    assert bench.traffic_from_profiles("ll_combine_kernel") is None
+        others = [w for w in bench.WORKLOAD_TEXT
+                  if not any(x["kernel"] == kernel and x["workload"] == w for x in entries)]
+        for w in others:
+            assert bench.traffic_from_profiles(kernel, w) is None
+    assert bench.traffic_from_profiles("no_such_kernel") is None
 
 
 def test_fp8_scale_names_match_the_abi():
