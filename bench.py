@@ -363,7 +363,7 @@ WORKLOAD_TEXT = {
     "group_limited": "dsv3 shape, 4-of-8 expert groups then top-8 inside them; layout + fused "
                      "e4m3 dispatch (per-128-channel fp32 scales) + weighted bf16 combine",
     "ll_decode": "R=8 x {T} tokens, hidden 7168, 256 experts, top-8 with 5% masked; low-latency "
-                 "e4m3 dispatch send phase, receive phase, weighted bf16 combine; Nmax=128",
+                 "e4m3 dispatch send phase, receive phase, weighted bf16 combine; Nmax={nmax}",
     "zipf_reuse": "R=16 x {T} tokens, hidden 4096, 128 experts, top-6 Zipf(1.2); layout once, "
                   "then dispatch(handle) of fresh x + weighted combine(handle)",
     "dsv3_expert_major": "dsv3 shape; layout with the expert-major placement + expert-major bf16 "
@@ -670,7 +670,7 @@ MAX_REPEATS = 2000
 def config_dict(name, w, units, world, l2):
     """The `config` object of a bench line (shared by the GPU and the reference arm)."""
     key = "valid_entries" if name in ("ll_decode", "ll_decode_packed", "dsv3_expert_major") else "recv_rows"
-    return {"workload": f"{name}: " + WORKLOAD_TEXT[name].format(T=w.T),
+    return {"workload": f"{name}: " + WORKLOAD_TEXT[name].format(T=w.T, nmax=w.nmax),
             "R": w.R, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "C": w.C, key: units,
             "parallelism": f"replicas x{world} (virtual EP{w.R} inside each GPU)", "l2": l2}
 
