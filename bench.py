@@ -91,7 +91,6 @@ KERNEL_SOURCES = {
     "ll_combine_kernel": ("ll.cu", "rowops.cuh", "ep_internal.cuh"),
     "dispatch_em_tma_kernel": ("expert_major.cu", "rowops.cuh", "ep_internal.cuh"),
     "combine_em_kernel": ("expert_major.cu", "rowops.cuh", "ep_internal.cuh"),
-    "layout_cluster_kernel": ("layout.cu", "ep_internal.cuh"),
 }
 
 
@@ -477,11 +476,7 @@ def make_plan(args, ep, dev, stream, launch):
 
         if not reuse:
             plan["layout_dispatch_synced"] = layout_dispatch_synced
-            # The layout runs as one cluster launch or as two kernels, by shape.
-            n0 = ep.ep_kernel_launch_count()
-            layout()
-            plan["layout_kernels"] = ("layout_cluster_kernel" if ep.ep_kernel_launch_count() - n0 == 1
-                                      else "layout_count+layout_prefix")
+            plan["layout_kernels"] = "layout_count+layout_prefix"
         dname = "dispatch_fp8" if fp8 else "dispatch"
         # The plan owns every buffer whose raw pointers the calls use.
         plan["keep"] = (lb, rb, y, out, xs)

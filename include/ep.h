@@ -217,7 +217,9 @@ typedef struct ep_recv {
  *                        (source, token) order, source s starting at the sum of the
  *                        counts of sources s' < s, so a grouped GEMM reads one
  *                        contiguous block per expert.
- * Either layout's send phase is two kernels: a per-source count, then the rows. */
+ * Either layout's send phase is two kernels: a per-source rank kernel (the in-source
+ * rank of every entry, in entry order, and the per-expert counts; linear in T*k), then
+ * the rows. */
 typedef enum ep_ll_layout { EP_LL_LAYOUT_SLOTS = 0, EP_LL_LAYOUT_PACKED = 1 } ep_ll_layout;
 
 /* Low-latency buffers and handle ([README] low-latency example; [HOOK]). All dev.

@@ -220,6 +220,10 @@ LL_CASES = {
     "long": W("ll", R=2, T=300, H=256, E=16, k=8, nmax=300, mask_p=0.05, seed=118),
     # rows longer than a send block loads up front (bf16 > 16 KB, e4m3 source > 16 KB)
     "wide": W("lw", R=2, T=20, H=16384, E=8, k=4, nmax=24, seed=119),
+    # the rank kernel's running counts across chunks: 8192 entries per source (8 chunks)
+    "chunks": W("lc", R=2, T=1024, H=128, E=64, k=8, nmax=1024, mask_p=0.05, seed=120),
+    # many experts: fewer warps per rank-kernel chunk (5 at E = 4096), 4 chunks per source
+    "experts4096": W("le", R=4, T=64, H=128, E=4096, k=8, nmax=64, mask_p=0.05, seed=121),
 }
 
 
