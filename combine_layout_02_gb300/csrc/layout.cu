@@ -243,15 +243,29 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
     int sum2 = 0;
     if (totals && a.num_tokens_per_expert != nullptr && p2 < R * E) {
         const int sp = p2 / E, e = p2 - sp * E;
-#pragma unroll 4
-        for (int cp = 0; cp < C; ++cp) sum2 += a.ws_expert[((int64_t)sp * C + cp) * E + e];
+        const int32_t* col = a.ws_expert + (int64_t)sp * C * E + e;
+        for (int c0 = 0; c0 < C; c0 += 16) {   // 16 loads in flight before the first add
+            int v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = c0 + q < C ? col[(int64_t)(c0 + q) * E] : 0;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) sum2 += v[q];
+        }
     }
     // (3) Per-expert receive totals: one expert per warp of the grid.
     const int e3 = totals ? b * kWarps + warp : E;
     int sum3 = 0;
     if (e3 < E) {
-#pragma unroll 4
-        for (int i = lane; i < R * C; i += 32) sum3 += a.ws_expert[(int64_t)i * E + e3];
+        for (int i0 = 0; i0 < R * C; i0 += 32 * 8) {   // 8 loads per lane in flight
+            int v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int i = i0 + q * 32 + lane;
+                v[q] = i < R * C ? a.ws_expert[(int64_t)i * E + e3] : 0;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sum3 += v[q];
+        }
     }
 
     // ---- Reductions and stores.
@@ -305,14 +319,20 @@ __global__ void __launch_bounds__(kThreads) layout_prefix_kernel(LayoutArgs a) {
             if (lane == 0) s_warp_tot[warp][d] = __popc(bal);
         }
         __syncthreads();
-        if (threadIdx.x < R) {
-            const int d = threadIdx.x;
-            int run = s_base[d];
-            for (int w = 0; w < kWarps; ++w) {
-                s_warp_off[w][d] = run;
-                run += s_warp_tot[w][d];
+        // Offsets of the warps per destination: one warp per destination scans the
+        // kWarps (16) warp totals with shuffles.
+        for (int d = warp; d < R; d += kWarps) {
+            const int v = lane < kWarps ? s_warp_tot[lane][d] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < kWarps; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += y;
             }
-            s_base[d] = run;
+            const int run = s_base[d];
+            if (lane < kWarps) s_warp_off[lane][d] = run + incl - v;
+            __syncwarp();
+            if (lane == kWarps - 1) s_base[d] = run + incl;
         }
         __syncthreads();
         const uint32_t lt = lanemask_lt();
