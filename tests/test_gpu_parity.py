@@ -613,3 +613,29 @@ def test_ll_repeated_experts_bit_exact(packed, use_fp8):
         np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
     np.testing.assert_array_equal(host_bits(buf.recv_x), exp["recv_x"])
     assert run.flags() == 0
+
+
+@pytest.mark.parametrize("packed", [False, True])
+@pytest.mark.parametrize("E", [4, 2048])
+def test_ll_repeated_experts_across_rank_chunks(packed, E):
+    """Repeated experts over many rank-kernel chunks: k = 5 entries per token from few
+    experts (E = 4), or from a large expert set where a chunk holds only a few warps
+    (E = 2048), T*k = 4000 entries per source, so equal experts meet across lanes, warps
+    and chunks. Every slot, count and range equals the oracle's."""
+    rng = np.random.default_rng(122 + E)
+    R, T, H, k = 2, 800, 128, 5
+    nmax = 4096 if E == 4 else 800
+    pool = np.array([0, 1, 2, 3]) if E == 4 else rng.choice(E, 12, replace=False)
+    topk = pool[rng.integers(0, len(pool), size=(R, T, k))].astype(np.int64)
+    topk[rng.random((R, T, k)) < 0.05] = -1
+    inp = {"x": workloads.make_hidden(rng, R, T, H), "topk_idx": topk,
+           "topk_weights": np.full((R, T, k), 1.0 / k, np.float32)}
+    run = GpuRun(R, T, H, E, k, 1, inp, nmax=nmax)
+    buf = run.ll_dispatch(True, packed=packed)
+    exp = oracle.ll_dispatch(inp["x"], topk, E, nmax, True, packed=packed, fill_x=0x5A)
+    assert exp["bad_entries"] == 0
+    for key in ("slot", "recv_expert_count", "layout_range", "src_info"):
+        np.testing.assert_array_equal(host_bits(getattr(buf, key)), exp[key], err_msg=key)
+    filled = exp["src_info"] != -7
+    np.testing.assert_array_equal(host_bits(buf.recv_x)[filled], exp["recv_x"][filled])
+    assert run.flags() == 0
