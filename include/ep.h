@@ -25,7 +25,8 @@
  * General rules for every call:
  *   - All pointers marked "dev" are device pointers owned by the caller; the library
  *     never allocates, frees or retains memory, and keeps no state between calls
- *     other than a per-device cache of the SM count and a launch counter.
+ *     other than per-device caches (the SM count, a kernel's shared-memory limit set
+ *     once, the static-scratch array's address per context) and a launch counter.
  *   - Calls are asynchronous on launch->stream and never synchronise the host,
  *     except the functions whose name ends in _sync.
  *   - Argument errors are detected on the host before anything is enqueued and
