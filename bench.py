@@ -94,13 +94,37 @@ KERNEL_SOURCES = {
 }
 
 
+def strip_comments(text: str) -> str:
+    """C/C++ source without its comments (string and character literals kept), so that
+    edits to comments do not read as a changed kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def source_digest(files):
-    """sha256 over the named kernel source files."""
+    """sha256 over the named kernel source files, comments removed."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "combine_layout_02_gb300", "csrc")
     for name in sorted(files):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + strip_comments(f.read()).encode())
     return h.hexdigest()
 
 
@@ -369,7 +393,7 @@ WORKLOAD_TEXT = {
                          "dispatch (one row per token-expert entry, grouped per local expert) + "
                          "weighted combine; worst-case regions R*T*min(k, E_loc) rows per rank",
     "ll_decode_packed": "ll_decode with the packed receive layout (no gaps between the sources' "
-                        "rows of an expert; send phase = per-source count kernel + send kernel)",
+                        "rows of an expert; send phase = per-source rank kernel + send kernel)",
     "dsv3_backward": "dsv3 shape; layout and forward dispatch once, then per step the backward "
                      "pair with the cached handle: combine_backward = dispatch of a fresh output "
                      "gradient, dispatch_backward = sum combine of the received gradient rows "

@@ -94,7 +94,7 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // library which itself returned from pdl_wait() before its pdl_trigger(): everything
 // ordered before that earlier kernel is then complete, so the later kernel may read
 // the call's inputs before its own wait (the low-latency send kernel does this after the
-// send phase's count kernel). pdl_trigger() lets the next kernel of the stream start
+// send phase's rank kernel). pdl_trigger() lets the next kernel of the stream start
 // launching. Both are no-ops for kernels launched without the
 // programmatic-serialization attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kRankThreads) ll_rank_kernel(LLArgs a) {
 
 // Blocks [0, R*T): one per source token. With the receive phase in the same call
 // (write_recv), blocks [R*T, R*T + R): destination d's recv_expert_count and
-// layout_range from the count kernel's signals.
+// layout_range from the rank kernel's signals.
 __global__ void __launch_bounds__(kSendThreads, kSendBlocksPerSm) ll_send_kernel(LLArgs a) {
     __shared__ int64_t s_e[EP_MAX_TOPK];
     __shared__ int64_t s_rows[EP_MAX_TOPK];

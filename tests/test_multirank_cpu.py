@@ -103,3 +103,14 @@ def test_fp8_scale_names_match_the_abi():
     # every phase a workload can time names the kernel its roofline would cite
     assert {"combine_backward", "dispatch_backward", "dispatch", "dispatch_fp8", "combine",
             "dispatch_em", "combine_em", "ll_send", "ll_recv", "ll_combine"} <= set(bench.PHASE_KERNEL)
+
+
+def test_source_digest_ignores_comments_only():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = 'int f() { return 1; } // one\n/* two */ const char* s = "// kept";\n'
+    b = 'int f() { return 1; } // changed\n/* other\n text */ const char* s = "// kept";\n'
+    c = 'int f() { return 2; } // one\n/* two */ const char* s = "// kept";\n'
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    assert '"// kept"' in bench.strip_comments(a)
