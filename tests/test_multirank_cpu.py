@@ -114,3 +114,26 @@ def test_source_digest_ignores_comments_only():
     assert bench.strip_comments(a) == bench.strip_comments(b)
     assert bench.strip_comments(a) != bench.strip_comments(c)
     assert '"// kept"' in bench.strip_comments(a)
+
+
+def test_reference_arm_line_has_the_gpu_arm_config(monkeypatch):
+    """The reference arm (the CPU oracle on a bounded token sample) reports the same
+    metric, unit and config object as the GPU arm's dsv3 line: the same workload string,
+    shape keys, received-row count (from the oracle's layout of the whole workload),
+    parallelism and L2 note."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import oracle
+    monkeypatch.setenv("EP_ORACLE_BUDGET_S", "0.5")
+
+    class A:
+        steps, warmup = 1, 3
+    res = bench.run_reference(A, 0, 1)
+    w = bench.WORKLOAD
+    inp = bench.workloads.make_workload(w, with_hidden=False)
+    N = int(oracle.layout(inp["topk_idx"], w.E, w.C)["rank_prefix_matrix"][-1].sum())
+    assert res["impl"] == "reference" and res["metric"] == bench.METRIC and res["unit"] == "GB/s"
+    assert res["config"] == bench.config_dict("dsv3", w, N, 1, bench.DSV3_L2)
+    assert res["config"]["recv_rows"] == N
+    assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["value"] == res["value"]
+    assert res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["cores"] == 1
