@@ -13,7 +13,9 @@ timed pass repeats its K steps until half a second of wall time has passed, so t
 nvidia-smi clock sampler sees the whole window under load; figures are means over all
 repeats (`repeats`, `timed_steps`). `dispatch_gbs`, `combine_gbs`, `layout_dispatch_us`
 and `roofline` come from a second timed pass of the same steps with CUDA events on the
-launching stream around every phase. `layout_dispatch_synced_us` is the exact-size
+launching stream around every phase; `layout_dispatch_region_us` from a third pass with
+one event before the layout and one after the dispatch (the dispatch chained to the layout
+kernels as in use). `layout_dispatch_synced_us` is the exact-size
 variant: layout, a host wait for the received counts, then the dispatch into regions of
 exactly those sizes. `e2e` is the same metric through the same C-ABI calls with host
 buffers: pinned host -> device copy of x / topk_idx / topk_weights and a device -> host
@@ -704,13 +706,17 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
     phases = plan["phases"]
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if plan["flush"] else None
 
-    def step(ev=None):
+    def step(ev=None, bounds=None):
+        """One step; with events, ev[j] is recorded before phase bounds[j] (every phase
+        when bounds is None) and the last event after the step."""
+        j = 0
         for i, (_, call) in enumerate(phases):
-            if ev is not None:
-                ev[i].record(stream)
+            if ev is not None and (bounds is None or i in bounds):
+                ev[j].record(stream)
+                j += 1
             call()
         if ev is not None:
-            ev[len(phases)].record(stream)
+            ev[j].record(stream)
 
     for _ in range(max(args.warmup, 3)):
         if flush_buf is not None:
@@ -720,16 +726,21 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
     nbytes, units = plan["nbytes"]()
     total_bytes = sum(nbytes.values())
 
-    def timed_window(sampler, per_phase, flush=True):
+    def timed_window(sampler, per_phase, flush=True, bounds=None):
         """Repeats of K steps between a barrier and a synchronisation on each side, until
         MIN_WINDOW_S have passed. per_phase=False (the headline pass): events only around
         each K-step region (around each step when L2 is flushed between steps, so the flush
         stays outside), so consecutive kernels overlap through programmatic dependent
-        launch as they do in use. per_phase=True (the breakdown pass): an event before and
-        after every phase. Returns (ms per step, per-phase ms lists, launches, clocks,
-        repeats)."""
+        launch as they do in use. per_phase=True (the breakdown pass): an event before
+        every phase (or before the phases listed in `bounds` only, timing the runs of
+        phases between them as one segment) and after the step. Returns (ms per step,
+        per-segment ms lists keyed by the segment's phase names joined with "+", launches,
+        clocks, repeats)."""
         n = args.steps
         fbuf = flush_buf if flush else None
+        cuts = list(range(len(phases))) if bounds is None else sorted(bounds)
+        seg_names = ["+".join(name for name, _ in phases[c:(cuts[j + 1] if j + 1 < len(cuts) else len(phases))])
+                     for j, c in enumerate(cuts)]
         barrier(world)
         torch.cuda.synchronize()
         n0 = ep.ep_kernel_launch_count()
@@ -737,10 +748,10 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
             sampler.start()
         t0 = time.perf_counter()
         total_ms, reps = 0.0, 0
-        per = {name: [] for name, _ in phases} if per_phase else None
+        per = {name: [] for name in seg_names} if per_phase else None
         while True:
             if per_phase:
-                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(n)]
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(cuts) + 1)] for _ in range(n)]
             elif fbuf is not None:
                 evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
             else:
@@ -752,7 +763,7 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
                 if fbuf is not None:
                     fbuf.zero_()
                 if per_phase:
-                    step(evs[i])
+                    step(evs[i], bounds)
                 elif evs is not None:
                     evs[i][0].record(stream)
                     step()
@@ -763,8 +774,8 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
             torch.cuda.synchronize()
             reps += 1
             if per_phase:
-                for i, (name, _) in enumerate(phases):
-                    per[name].extend(e[i].elapsed_time(e[i + 1]) for e in evs)
+                for j, name in enumerate(seg_names):
+                    per[name].extend(e[j].elapsed_time(e[j + 1]) for e in evs)
             if evs is not None:
                 total_ms += sum(e[0].elapsed_time(e[-1]) for e in evs)
             else:
@@ -784,6 +795,14 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
     # Per-phase breakdown (and the roofline's per-kernel durations): a second timed pass of
     # the same steps with an event around every phase.
     phase_ms, per, _, phase_clocks, phase_reps = timed_window(ClockSampler(gpu_id), per_phase=True)
+    # Layout and dispatch as one region (the dispatch chained to the layout kernels by
+    # programmatic dependent launch, as in use): events before the layout, before the phase
+    # after the dispatch, and after the step.
+    region_us = None
+    names = phases_names(phases)
+    if len(names) >= 2 and names[0] == "layout" and names[1].startswith("dispatch"):
+        _, seg, _, _, _ = timed_window(None, per_phase=True, bounds=(0, 2) if len(names) > 2 else (0,))
+        region_us = round(reduce_max(statistics.mean(seg[f"layout+{names[1]}"]), world, dev) * 1e3, 2)
     warm = None
     if flush_buf is not None:
         # Small working sets may stay in L2 between steps in use: the same steps unflushed.
@@ -830,6 +849,8 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
     if "layout" in mean_ms:
         dname = next(n for n in mean_ms if n.startswith("dispatch"))
         result["layout_dispatch_us"] = round((mean_ms["layout"] + mean_ms[dname]) * 1e3, 2)
+    if region_us is not None:
+        result["layout_dispatch_region_us"] = region_us
     result["bytes_per_step"] = nbytes
     result["roofline"] = {"bound": "hbm", "kernel": kernels[dom], "achieved": round(gbs[dom], 1),
                           "peak": peak, "unit": "GB/s", "frac": round(gbs[dom] / peak, 4),
@@ -846,7 +867,10 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
                         f"{args.min_window_s} s of wall time had passed ({reps} repeats, "
                         f"{reps * args.steps} steps; the mean over all of them); *_us, *_gbs and "
                         "roofline: a second pass with an event around every phase "
-                        f"({phase_reps} repeats; its step: {phase_ms:.4f} ms)")
+                        f"({phase_reps} repeats; its step: {phase_ms:.4f} ms); "
+                        "layout_dispatch_us: the sum of the layout and dispatch phases of that pass; "
+                        "layout_dispatch_region_us: a third pass with one event before the layout "
+                        "and one after the dispatch")
     result["repeats"] = reps
     result["timed_steps"] = reps * args.steps
     result["gpu_launches"] = launches
@@ -865,7 +889,7 @@ def phases_names(phases):
 EXTRA_WORKLOADS = ("group_limited", "zipf_reuse", "ll_decode")
 EXTRA_KEYS = ("value", "unit", "ms_per_step", "config", "layout_us", "dispatch_us", "dispatch_gbs",
               "dispatch_frac_of_peak", "combine_us", "combine_gbs", "combine_frac_of_peak",
-              "layout_dispatch_us", "ll_send_us", "ll_send_gbs", "ll_send_frac_of_peak", "ll_recv_us",
+              "layout_dispatch_us", "layout_dispatch_region_us", "ll_send_us", "ll_send_gbs", "ll_send_frac_of_peak", "ll_recv_us",
               "ll_combine_us", "ll_combine_gbs", "ll_combine_frac_of_peak", "bytes_per_step",
               "roofline", "warm", "graph", "repeats", "timed_steps", "gpu_launches", "clocks",
               "phase_pass_clocks", "clocks_remeasured", "layout_dispatch_synced_us")

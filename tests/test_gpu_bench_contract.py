@@ -45,6 +45,8 @@ def test_bench_line_dsv3_small():
     _common(d)
     assert d["config"]["workload"].startswith("dsv3:") and d["config"]["T"] == 256
     assert set(d["bytes_per_step"]) == {"layout", "dispatch", "combine"}
+    # layout + dispatch as one event-bounded region, and as the sum of the two phases
+    assert 0 < d["layout_dispatch_region_us"] and 0 < d["layout_dispatch_us"]
     # layout + dispatch + combine launches per step (the layout is two kernels)
     assert d["gpu_launches_per_step"] == 4
     e2e = d["e2e"]
