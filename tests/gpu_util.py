@@ -49,6 +49,35 @@ def assert_close_bf16_dev(got: torch.Tensor, exp_bits: np.ndarray, atol=ATOL, rt
                                  f"{i}; first at flat index {first}")
 
 
+U_FP32 = 2.0 ** -24             # unit roundoff of binary32
+
+
+def assert_weight_sums_close(got, exp, recv_topk_weights, send_head, row_offset):
+    """combined_topk_weights against the oracle. The kernel adds each token's received
+    weights in fp32, one destination row after another (n terms); the oracle adds them in
+    binary64 and rounds once. The recursive-summation bound (Higham, "Accuracy and Stability
+    of Numerical Algorithms", 2nd ed., section 4.2) gives, per element,
+        |got - exact| <= (n - 1) u sum_i |x_i| / (1 - (n - 1) u),   u = 2^-24,
+    and the oracle's rounding adds at most u |exp|; the test allows that plus 1 %."""
+    got = np.asarray(got, np.float64)
+    exp = np.asarray(exp, np.float64)
+    R, T = send_head.shape[0], send_head.shape[1]
+    k = recv_topk_weights.shape[1]
+    got, exp = got.reshape(R, T, k), exp.reshape(R, T, k)
+    sabs = np.zeros((R, T, k))
+    n = np.zeros((R, T, 1))
+    for d in range(R):
+        h = send_head[:, :, d]
+        m = h >= 0
+        sabs[m] += np.abs(recv_topk_weights[int(row_offset[d]) + h[m]].astype(np.float64))
+        n[m] += 1
+    g = np.maximum(n - 1, 0) * U_FP32
+    tol = (g / (1 - g) * sabs + U_FP32 * np.abs(exp)) * 1.01 + 1e-37
+    bad = np.abs(got - exp) > tol
+    assert not bad.any(), (f"{int(bad.sum())} weight sums outside the fp32 summation bound; first at "
+                           f"{np.argwhere(bad)[0]}: {got[bad][0]} vs {exp[bad][0]}")
+
+
 def compact_offsets(rank_prefix: np.ndarray) -> list:
     off = [0]
     for n in rank_prefix[-1]:

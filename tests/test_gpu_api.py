@@ -10,7 +10,7 @@ import combine_layout_02_gb300 as ep
 from combine_layout_02_gb300.api import Buffer
 import oracle
 import workloads
-from gpu_util import assert_close_bf16, dev_bf16, host_bits
+from gpu_util import assert_close_bf16, dev_bf16, host_bits, assert_weight_sums_close
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,8 @@ def test_buffer_normal_path_matches_the_oracle():
                         oracle.COMBINE_WEIGHTED, inp["topk_idx"], inp["topk_weights"],
                         recv_topk_weights=exp["recv_topk_weights"])
     assert_close_bf16(host_bits(out), ec["out"])
-    np.testing.assert_allclose(cw.cpu().numpy(), ec["combined_topk_weights"], rtol=1e-5, atol=1e-6)
+    assert_weight_sums_close(cw.cpu().numpy(), ec["combined_topk_weights"], exp["recv_topk_weights"],
+                             ref["send_head"], off)
 
     # handle reuse with fresh x, then a plain-sum combine of one tensor of rows
     rng = np.random.default_rng(502)

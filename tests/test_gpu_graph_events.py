@@ -21,7 +21,7 @@ import combine_layout_02_gb300 as ep
 from combine_layout_02_gb300.buffers import LayoutBuffers, LLBuffers, RecvBuffers, new_event
 import oracle
 import workloads
-from gpu_util import GpuRun, assert_close_bf16, bf16_to_f64, compact_offsets, dev_bf16, host_bits
+from gpu_util import GpuRun, assert_close_bf16, bf16_to_f64, compact_offsets, dev_bf16, host_bits, assert_weight_sums_close
 
 pytestmark = pytest.mark.gpu
 
@@ -210,7 +210,7 @@ def test_backward_identities_exact_on_integer_data():
     _, cw = run.combine(yd, off, ep.EP_COMBINE_SUM, recv_topk_weights=torch.from_numpy(gw).cuda())
     exp = oracle.combine(yd.view(torch.int16).cpu().numpy().view(np.uint16), ref["send_head"],
                          np.array(off), W.E, W.k, recv_topk_weights=gw)["combined_topk_weights"]
-    np.testing.assert_allclose(cw.cpu().numpy(), exp, rtol=1e-5, atol=1e-6)
+    assert_weight_sums_close(cw.cpu().numpy(), exp, gw, ref["send_head"], off)
 
 
 def test_event_overlap_helpers_order_like_the_raw_events():

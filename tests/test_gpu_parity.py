@@ -15,7 +15,7 @@ import torch
 import combine_layout_02_gb300 as ep
 import oracle
 import workloads
-from gpu_util import GpuRun, assert_close_bf16, bf16_to_f64, compact_offsets, dev_bf16, host_bits
+from gpu_util import GpuRun, assert_close_bf16, bf16_to_f64, compact_offsets, dev_bf16, host_bits, assert_weight_sums_close
 
 pytestmark = pytest.mark.gpu
 
@@ -152,7 +152,8 @@ def test_combine_within_tolerance(name, mode):
     exp = oracle.combine(ybits, ref["send_head"], np.array(off), w.E, w.k, mode,
                          inp["topk_idx"], inp["topk_weights"], recv_topk_weights=rtw[: off[-1]])
     assert_close_bf16(host_bits(out), exp["out"])
-    np.testing.assert_allclose(cw.cpu().numpy(), exp["combined_topk_weights"], rtol=1e-5, atol=1e-6)
+    assert_weight_sums_close(cw.cpu().numpy(), exp["combined_topk_weights"], rtw[: off[-1]],
+                             ref["send_head"], off)
     assert run.flags() == 0
 
 
