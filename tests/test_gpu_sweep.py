@@ -1,4 +1,5 @@
-"""Seeded sweep of random small shapes through every entry point, against the oracle.
+"""Seeded sweep of random small shapes through every entry point, against the oracle
+(three sets: small shapes, wide rows with capped grids, many experts per rank).
 
 Each case draws R (1 to 64, including primes), experts per rank, k (1 to 32), T
 (including 0, 1 and non-multiples of the channel and tile sizes), H, C, masking and
@@ -49,7 +50,36 @@ def _draw_cases(n=24, seed=2024, name="sweep", wide=False):
     return cases
 
 
-CASES = _draw_cases() + _draw_cases(16, seed=2025, name="wide", wide=True)
+def _draw_cases_many_experts(n=12, seed=2026, name="manyexp"):
+    """Many experts per rank (16 to 256, E up to 8192), rows up to 7168 wide, 1 to 24
+    channels, masking up to one entry in two, and uniform, Zipf or group-limited routing."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        R = int(rng.choice([2, 3, 4, 6, 8, 12, 16]))
+        E_loc = min(int(rng.choice([16, 32, 64, 128, 256])), 8192 // R)
+        E = R * E_loc
+        k = int(rng.integers(1, min(E, 32) + 1))
+        T = int(rng.choice([1, 3, 31, 64, 200, 513]))
+        H = int(rng.choice([128, 512, 1536, 4096, 7168]))
+        if R * T * H > (1 << 24):
+            H = 512
+        C = int(rng.integers(1, 25))
+        mask_p = float(rng.choice([0.0, 0.05, 0.5]))
+        routing = str(rng.choice(["uniform", "zipf", "group"]))
+        kw = {}
+        if routing == "group":
+            kw = dict(groups=R, topk_groups=int(rng.integers(1, R + 1)))
+            k = min(k, kw["topk_groups"] * E_loc)
+        sms = int(rng.choice([0, 0, 3, 40]))
+        cases.append((workloads.Workload(f"{name}{i}", R=R, T=T, H=H, E=E, k=k, C=C, mask_p=mask_p,
+                                         routing=routing, zipf_s=1.2 if routing == "zipf" else 0.0,
+                                         nmax=T + int(rng.integers(0, 3)), seed=7000 + i, **kw), sms))
+    return cases
+
+
+CASES = (_draw_cases() + _draw_cases(16, seed=2025, name="wide", wide=True)
+         + _draw_cases_many_experts())
 
 
 def _ids(case):
