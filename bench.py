@@ -739,8 +739,7 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
         n = args.steps
         fbuf = flush_buf if flush else None
         cuts = list(range(len(phases))) if bounds is None else sorted(bounds)
-        seg_names = ["+".join(name for name, _ in phases[c:(cuts[j + 1] if j + 1 < len(cuts) else len(phases))])
-                     for j, c in enumerate(cuts)]
+        seg_names = segment_names(phases_names(phases), cuts)
         barrier(world)
         torch.cuda.synchronize()
         n0 = ep.ep_kernel_launch_count()
@@ -883,6 +882,14 @@ def measure_workload(args, world, dev, ep, err, stream, launch, gpu_id):
 
 def phases_names(phases):
     return [name for name, _ in phases]
+
+
+def segment_names(names, cuts):
+    """Names of the timed segments when events are recorded before the phases at the
+    sorted indices `cuts` and after the last phase: each segment runs from one cut to the
+    next and is named by its phases joined with "+"."""
+    ends = list(cuts[1:]) + [len(names)]
+    return ["+".join(names[c:e]) for c, e in zip(cuts, ends)]
 
 
 # The extra workloads the default (dsv3) line also measures, each in its own object.

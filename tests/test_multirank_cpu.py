@@ -137,3 +137,12 @@ def test_reference_arm_line_has_the_gpu_arm_config(monkeypatch):
     assert res["config"]["recv_rows"] == N
     assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["value"] == res["value"]
     assert res["cpu_baseline"]["kind"] == "oracle" and res["cpu_baseline"]["cores"] == 1
+
+
+def test_segment_names_of_the_timed_passes():
+    import bench
+    names = ["layout", "dispatch", "combine"]
+    assert bench.segment_names(names, [0, 1, 2]) == names
+    assert bench.segment_names(names, [0, 2]) == ["layout+dispatch", "combine"]
+    assert bench.segment_names(names, [0]) == ["layout+dispatch+combine"]
+    assert bench.segment_names(["layout", "dispatch_fp8"], [0]) == ["layout+dispatch_fp8"]
