@@ -12,7 +12,9 @@
 // (ascending rank order) and their coefficients (1, or the sum of the token's weights
 // whose experts live on that rank), then accumulates in fp32 registers and stores
 // bf16 once. Each received row is read exactly once, with 32-byte loads when y is
-// 32-byte aligned (16-byte loads otherwise).
+// 32-byte aligned (16-byte loads otherwise). The batch shape (units per lane U, rows
+// P) and the blocks kept resident per SM follow the row length and the rows per token,
+// so that enough bytes are in flight per SM (see combine_form).
 #include "rowops.cuh"
 
 namespace ep {
@@ -60,8 +62,8 @@ __device__ __forceinline__ TokenMeta load_meta(const CombineArgs& a, int64_t g, 
     return m;
 }
 
-template <int U, int P, bool V32>
-__global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
+template <int U, int P, bool V32, int MIN_BLOCKS = 0>
+__global__ void __launch_bounds__(kThreads, MIN_BLOCKS) combine_kernel(CombineArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
     __shared__ float s_coef[kWarps][EP_MAX_RANKS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -125,6 +127,21 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a) {
     pdl_trigger();
 }
 
+// The kernel form for a shape. Short rows leave a token's gather with few bytes per lane,
+// so those forms trade load registers for resident warps (A/B on GB300, fraction of the
+// copy bandwidth, 2 units x 4 rows -> the chosen form, top-8 unless noted): H = 256
+// 0.33 -> 0.77, H = 512 0.61 -> 0.96, H = 1024 0.95 -> 1.04; at most two rows per token
+// (k <= 2 or R <= 2, H 4096-7168) 0.95-0.97 -> 1.01-1.02. Wider rows with more rows per
+// token keep 2 units x 4 rows at 126 registers (four 128-thread blocks per SM).
+using CombineKernel = void (*)(CombineArgs);
+CombineKernel combine_form(int H, int k, int R, bool y32) {
+    if (H <= 256) return combine_kernel<1, 4, false, 10>;   // 16-byte units: one per lane
+    if (!y32) return combine_kernel<kU, kP, false>;
+    if (H <= 1024) return combine_kernel<1, 4, true, 8>;    // one 32-byte unit per lane per row
+    if (k <= 2 || R <= 2) return combine_kernel<kU32, 2, true, 5>;
+    return combine_kernel<kU32, kP32, true>;
+}
+
 }  // namespace
 }  // namespace ep
 
@@ -172,8 +189,7 @@ extern "C" ep_status ep_combine(const ep_shape* sh, const void* y, const int64_t
 
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (ntok > 0) {
-        void (*kernel)(CombineArgs) = (((uintptr_t)y & 31) == 0) ? combine_kernel<kU32, kP32, true>
-                                                                  : combine_kernel<kU, kP, false>;
+        const CombineKernel kernel = combine_form(a.H, a.k, a.R, ((uintptr_t)y & 31) == 0);
         int64_t blocks = (ntok + kWarps - 1) / kWarps;
         if (sh->num_sms > 0) {
             int per_sm = 0;

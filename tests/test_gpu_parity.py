@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle, element by
 element, on seeded inputs spanning several tiles and ragged tails: the tiny workload,
 ragged shapes, R not a multiple of 8, R > 32, R = 1, R = 64, k = 32, every expert chosen,
-8192 experts, 16384-wide rows, empty inputs, masked entries, skewed and group-limited
-routing.
+8192 experts, 16384-wide rows, top-2 and two-rank shapes (at most two rows per token),
+empty inputs, masked entries, skewed and group-limited routing.
 
 Bit-exact: every layout / handle tensor, receive rows (bf16 and e4m3), FP8 scales,
 recv_topk_idx / recv_topk_weights / recv_src_idx, low-latency slots and counts, and
@@ -35,6 +35,8 @@ CASES = {
     "e8192": W("e8k", R=16, T=50, H=128, E=8192, k=8, C=3, seed=115),       # most experts
     "h16k": W("h16k", R=4, T=33, H=16384, E=16, k=4, C=2, seed=116),       # 32 KB rows
     "k_all": W("kall", R=4, T=40, H=256, E=32, k=32, C=5, seed=117),       # every expert
+    "top2_h4096": W("t2", R=8, T=300, H=4096, E=64, k=2, C=5, seed=119),   # <= 2 rows per token
+    "r2_h2048": W("r2w", R=2, T=200, H=2048, E=8, k=4, C=3, seed=120),    # <= 2 rows per token
 }
 
 
@@ -531,10 +533,13 @@ def test_rows_too_wide_for_bulk_copies_use_the_register_copy():
     assert run.flags() == 0
 
 
-def test_combine_16_byte_aligned_y_takes_the_16_byte_gather():
-    """y that is 16- but not 32-byte aligned uses the 16-byte-load gather (aligned y uses
-    32-byte loads): both match the oracle, rank-major and expert-major."""
-    w, inp, run, ref = _setup("zipf16")
+@pytest.mark.parametrize("name", ["zipf16", "tiny", "h16k", "top2_h4096"])
+def test_combine_16_byte_aligned_y_takes_the_16_byte_gather(name):
+    """y that is 16- but not 32-byte aligned uses a 16-byte-load gather (aligned y uses
+    32-byte loads): both match the oracle, rank-major and expert-major, for each form of the
+    combine (rows of at most 256 channels, rows up to 1024, at most two rows per token, the
+    rest)."""
+    w, inp, run, ref = _setup(name)
     run.layout()
     off = compact_offsets(ref["rank_prefix_matrix"])
     rng = np.random.default_rng(w.seed + 4000)
