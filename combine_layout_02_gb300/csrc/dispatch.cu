@@ -114,8 +114,8 @@ __device__ __forceinline__ void copy_scale_rows(const DispatchArgs& a, int64_t g
         for (int i = lane; i < G; i += 32) rs[s_row[p] * G + i] = ss[i];
 }
 
-template <int MODE, int U, bool V32 = false>
-__global__ void __launch_bounds__(kThreads, 3) dispatch_kernel(DispatchArgs a) {
+template <int MODE, int U, bool V32 = false, int MIN_BLOCKS = 3>
+__global__ void __launch_bounds__(kThreads, MIN_BLOCKS) dispatch_kernel(DispatchArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_RANKS];
     __shared__ int s_dst[kWarps][EP_MAX_RANKS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -179,19 +179,19 @@ __global__ void __launch_bounds__(kTmaWarps * 32) dispatch_tma_kernel(DispatchAr
     pdl_trigger();
 }
 
-template <int MODE, int U, bool V32 = false>
+template <int MODE, int U, bool V32 = false, int MIN_BLOCKS = 3>
 ep_status launch_dispatch(const DispatchArgs& a, int num_sms, cudaStream_t stream) {
     if (a.ntok == 0) return EP_OK;
     int64_t blocks = (a.ntok + kWarps - 1) / kWarps;
     if (num_sms > 0) {
         int per_sm = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<MODE, U, V32>, kThreads, 0);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel<MODE, U, V32, MIN_BLOCKS>, kThreads, 0);
         if (e != cudaSuccess) return cuda_fail(e);
         const int64_t cap = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
         if (blocks > cap) blocks = cap;
     }
     if (blocks > 0x7FFFFFFF) blocks = 0x7FFFFFFF;
-    cudaError_t e = launch_pdl(dispatch_kernel<MODE, U, V32>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
+    cudaError_t e = launch_pdl(dispatch_kernel<MODE, U, V32, MIN_BLOCKS>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, a);
     return e == cudaSuccess ? EP_OK : cuda_fail(e);
 }
 
@@ -289,8 +289,19 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     a.err = launch->error_flags;
 
     if ((st = begin_call(launch)) != EP_OK) return st;
-    if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3 && ((uintptr_t)x & 31) == 0)
-        st = launch_dispatch<kQuant, 2, true>(a, sh->num_sms, launch->stream);   // 32-byte loads
+    // Fused e4m3 with 32-byte loads. Short rows (a lane's one unit per row) and tokens with
+    // at most two destinations trade load registers for resident warps (A/B on GB300, top-8
+    // unless noted, fraction of the copy bandwidth: H = 1024 0.76 -> 0.90, H = 512 0.51 ->
+    // 0.68; top-2 with H = 4096 0.945 -> 0.976); rows with more destinations keep 2 units
+    // per lane at three blocks per SM (four measured slower there: 0.934 -> 0.917 on the
+    // DeepSeek-V3 shape with uniform top-8).
+    const bool fp8_32 = x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3 && ((uintptr_t)x & 31) == 0;
+    if (fp8_32 && a.H <= 1024)
+        st = launch_dispatch<kQuant, 1, true, 5>(a, sh->num_sms, launch->stream);
+    else if (fp8_32 && (a.k <= 2 || a.R <= 2))
+        st = launch_dispatch<kQuant, 2, true, 4>(a, sh->num_sms, launch->stream);
+    else if (fp8_32)
+        st = launch_dispatch<kQuant, 2, true>(a, sh->num_sms, launch->stream);
     else if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)
         st = launch_dispatch<kQuant, 2>(a, sh->num_sms, launch->stream);
     else if (tma_copy_fits(a))

@@ -17,6 +17,8 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCopyU = 8, kQuantU = 2, kGatherU = 4, kGatherP = 4;
+constexpr int kCombineThreads = 128;    // combine: 4 warps per block, as the rank-major one
+constexpr int kCombineWarps = kCombineThreads / 32;
 
 struct EmArgs {
     const char* x;
@@ -127,25 +129,39 @@ __global__ void __launch_bounds__(kTmaWarps * 32) dispatch_em_tma_kernel(EmArgs 
     pdl_trigger();
 }
 
-template <bool V32>
-__global__ void __launch_bounds__(kThreads) combine_em_kernel(EmArgs a) {
-    __shared__ int64_t s_row[kWarps][EP_MAX_TOPK];
-    __shared__ float s_coef[kWarps][EP_MAX_TOPK];
+// The batch shape (units per lane U, rows P) and resident blocks per SM follow the row
+// length and the entries per token, as in the rank-major combine (combine_em_form).
+template <int U, int P, bool V32, int MIN_BLOCKS = 0>
+__global__ void __launch_bounds__(kCombineThreads, MIN_BLOCKS) combine_em_kernel(EmArgs a) {
+    __shared__ int64_t s_row[kCombineWarps][EP_MAX_TOPK];
+    __shared__ float s_coef[kCombineWarps][EP_MAX_TOPK];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t nw = (int64_t)gridDim.x * kWarps;
+    const int64_t nw = (int64_t)gridDim.x * kCombineWarps;
     pdl_wait();
-    for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
+    for (int64_t g = (int64_t)blockIdx.x * kCombineWarps + warp; g < a.ntok; g += nw) {
         const int nd = entry_rows(a, g, lane, s_row[warp], s_coef[warp]);
         __syncwarp();
         if (V32)
-            gather_reduce_row32<2, 4>(a.y, s_row[warp], s_coef[warp], nd, a.H,
+            gather_reduce_row32<U, P>(a.y, s_row[warp], s_coef[warp], nd, a.H,
                                       a.out + g * (int64_t)a.H * 2, lane, 32);
         else
-            gather_reduce_row<kGatherU, kGatherP>(a.y, s_row[warp], s_coef[warp], nd, a.H,
-                                              a.out + g * (int64_t)a.H * 2, lane, 32);
+            gather_reduce_row<U, P>(a.y, s_row[warp], s_coef[warp], nd, a.H,
+                                    a.out + g * (int64_t)a.H * 2, lane, 32);
         __syncwarp();
     }
     pdl_trigger();
+}
+
+// Rows of at most 256 channels: 16-byte units, one per lane; up to 1024 channels: one
+// 32-byte unit per lane per row; at most two entries per token: 2 rows per batch; the
+// rest 2 units x 4 rows. The short-row and two-row forms keep more blocks resident.
+using CombineEmKernel = void (*)(EmArgs);
+CombineEmKernel combine_em_form(int H, int k, bool y32) {
+    if (H <= 256) return combine_em_kernel<1, 4, false, 10>;
+    if (!y32) return combine_em_kernel<kGatherU, kGatherP, false>;
+    if (H <= 1024) return combine_em_kernel<1, 4, true, 8>;
+    if (k <= 2) return combine_em_kernel<2, 2, true, 5>;
+    return combine_em_kernel<2, 4, true>;
 }
 
 ep_status em_common(const ep_shape* sh, const ep_handle* handle, const int64_t* topk_idx,
@@ -250,11 +266,10 @@ ep_status ep_combine_expert_major(const ep_shape* sh, const void* y, const int64
     a.topk_weights = mode == EP_COMBINE_WEIGHTED ? topk_weights : nullptr;
     if ((st = begin_call(launch)) != EP_OK) return st;
     if (a.ntok > 0) {
-        const unsigned blocks = (unsigned)((a.ntok + kWarps - 1) / kWarps);
+        const unsigned blocks = (unsigned)((a.ntok + kCombineWarps - 1) / kCombineWarps);
         // 32-byte loads when y is 32-byte aligned (as the rank-major combine).
-        cudaError_t e = ((uintptr_t)y & 31) == 0
-                            ? launch_pdl(combine_em_kernel<true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a)
-                            : launch_pdl(combine_em_kernel<false>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+        cudaError_t e = launch_pdl(combine_em_form(a.H, a.k, ((uintptr_t)y & 31) == 0), dim3(blocks),
+                                   dim3(kCombineThreads), 0, launch->stream, a);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     return end_call(launch);

@@ -75,8 +75,11 @@ def test_dispatch_bf16_bit_exact(name, offsets):
     assert run.flags() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "r3_odd", "group8", "r33", "k32"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "r3_odd", "group8", "r33", "k32", "h16k",
+                                  "top2_h4096", "r2_h2048"])
 def test_dispatch_fp8_fused_bit_exact(name):
+    """Every form of the fused quantisation: rows up to 1024 channels, at most two
+    destinations per token, and the rest."""
     w, inp, run, ref = _setup(name)
     run.layout()
     off = compact_offsets(ref["rank_prefix_matrix"])
@@ -323,7 +326,7 @@ def _cmp_scales(got, exp, mode):
         np.testing.assert_array_equal(got.view(np.uint32), exp.view(np.uint32))
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "group8", "k32"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "group8", "k32", "h16k", "top2_h4096"])
 @pytest.mark.parametrize("mode,ts", MODES)
 def test_dispatch_fp8_scale_modes_bit_exact(name, mode, ts):
     """round_scale / UE8M0 / per-tensor scale ("DeepEP" README feature notes)."""
