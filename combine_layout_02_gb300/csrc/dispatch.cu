@@ -19,7 +19,8 @@
 //                            stores it (rows up to 50 KB);
 //   dispatch_kernel<copy>    the same copy with 16-byte vector loads / stores (wider rows);
 //   dispatch_kernel<quant>   fused e4m3 quantisation, software-pipelined row loads
-//                            (32-byte loads when x is 32-byte aligned).
+//                            (32-byte loads when x is 32-byte aligned; pairs of units
+//                            with 32-byte stores when the receive rows are too).
 #include "rowops.cuh"
 
 namespace ep {
@@ -28,7 +29,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-enum { kCopy = 0, kQuant = 1 };
+enum { kCopy = 0, kQuant = 1, kQuantPair = 2 };
 
 struct DispatchArgs {
     const char* x;
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) dispatch_kernel(Dispatch
     __shared__ int s_dst[kWarps][EP_MAX_RANKS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nw = (int64_t)gridDim.x * kWarps;
-    const int64_t out_row_bytes = (int64_t)a.H * (MODE == kQuant ? 1 : a.in_elem);
+    const int64_t out_row_bytes = (int64_t)a.H * (MODE == kCopy ? a.in_elem : 1);
     pdl_wait();
 
     for (int64_t g = (int64_t)blockIdx.x * kWarps + warp; g < a.ntok; g += nw) {
@@ -129,7 +130,9 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) dispatch_kernel(Dispatch
         // Quantising: the row's first batch does not depend on the metadata, so its load
         // shares the metadata's memory round trip.
         uint4 qa[U], qb[U];
+        u32x8 qp[2];
         if (MODE == kQuant) quant_load<U, V32>(src, a.H >> 4, 0, lane, 32, qa, qb);
+        if (MODE == kQuantPair) pair_load(src, a.H >> 5, lane, qp);
 
         const int nd = token_rows_and_meta(a, g, t, lane, s_row[warp], s_dst[warp]);
 
@@ -137,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) dispatch_kernel(Dispatch
         if (MODE == kCopy) {
             scatter_copy_row<U>(src, a.recv_x, s_row[warp], nd, out_row_bytes, lane, 32);
             if (a.copy_scales) copy_scale_rows(a, g, s_row[warp], nd, lane);
+        } else if (MODE == kQuantPair) {
+            scatter_quant_pairs_loaded(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
+                                       s_row[warp], nd, a.H, a.qm, lane, qp);
         } else {
             scatter_quant_row_loaded<U, V32>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
                                              s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
@@ -292,14 +298,17 @@ extern "C" ep_status ep_dispatch(const ep_shape* sh, const void* x, ep_dtype x_d
     // Fused e4m3 with 32-byte loads. Short rows (a lane's one unit per row) and tokens with
     // at most two destinations trade load registers for resident warps (A/B on GB300, top-8
     // unless noted, fraction of the copy bandwidth: H = 1024 0.76 -> 0.90, H = 512 0.51 ->
-    // 0.68; top-2 with H = 4096 0.945 -> 0.976); rows with more destinations keep 2 units
-    // per lane at three blocks per SM (four measured slower there: 0.934 -> 0.917 on the
-    // DeepSeek-V3 shape with uniform top-8).
+    // 0.68; top-2 with H = 4096 0.945 -> 0.976). Rows with more destinations go by pairs of
+    // units (one 32-byte store per destination and two shuffles per group instead of two
+    // 16-byte stores and three: group_limited 0.980 -> 0.997, uniform top-8 0.934 -> 0.958)
+    // when the receive rows are 32-byte aligned, else by units at three blocks per SM.
     const bool fp8_32 = x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3 && ((uintptr_t)x & 31) == 0;
     if (fp8_32 && a.H <= 1024)
         st = launch_dispatch<kQuant, 1, true, 5>(a, sh->num_sms, launch->stream);
     else if (fp8_32 && (a.k <= 2 || a.R <= 2))
         st = launch_dispatch<kQuant, 2, true, 4>(a, sh->num_sms, launch->stream);
+    else if (fp8_32 && ((uintptr_t)out->recv_x & 31) == 0)
+        st = launch_dispatch<kQuantPair, 1, true>(a, sh->num_sms, launch->stream);
     else if (fp8_32)
         st = launch_dispatch<kQuant, 2, true>(a, sh->num_sms, launch->stream);
     else if (x_dtype == EP_BF16 && recv_dtype == EP_FP8_E4M3)

@@ -45,6 +45,14 @@ __device__ __forceinline__ u32x8 ld_stream_v8(const void* p) {
     return v;
 }
 
+// 32-byte store (sm_100+ st .v8.b32); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_v8(void* p, const u32x8& v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v.r[0]),
+                 "r"(v.r[1]), "r"(v.r[2]), "r"(v.r[3]), "r"(v.r[4]), "r"(v.r[5]), "r"(v.r[6]),
+                 "r"(v.r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_stream_v4(void* p, const uint4& v) {
     // Streaming store (evict-first): the written rows are far larger than L2.
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),

@@ -66,7 +66,9 @@ __device__ __forceinline__ int entry_rows(const EmArgs& a, int64_t g, int lane, 
     return __popc(bal);
 }
 
-template <bool QUANT, bool V32 = false>
+// QUANT: fused e4m3, by units (PAIRS false) or by pairs of units with 32-byte stores
+// (PAIRS true: x and the receive rows 32-byte aligned).
+template <bool QUANT, bool V32 = false, bool PAIRS = false>
 __global__ void __launch_bounds__(kThreads) dispatch_em_kernel(EmArgs a) {
     __shared__ int64_t s_row[kWarps][EP_MAX_TOPK];
     __shared__ float s_coef[kWarps][EP_MAX_TOPK];
@@ -77,7 +79,9 @@ __global__ void __launch_bounds__(kThreads) dispatch_em_kernel(EmArgs a) {
         const int t = (int)(g % a.T);
         const char* src = a.x + g * (int64_t)a.H * 2;
         uint4 qa[kQuantU], qb[kQuantU];   // quantising: first batch loaded with the metadata
-        if (QUANT) quant_load<kQuantU, V32>(src, a.H >> 4, 0, lane, 32, qa, qb);
+        u32x8 qp[2];
+        if (QUANT && PAIRS) pair_load(src, a.H >> 5, lane, qp);
+        else if (QUANT) quant_load<kQuantU, V32>(src, a.H >> 4, 0, lane, 32, qa, qb);
         const int nd = entry_rows(a, g, lane, s_row[warp], s_coef[warp]);
         __syncwarp();
         if (lane < nd) {
@@ -85,7 +89,10 @@ __global__ void __launch_bounds__(kThreads) dispatch_em_kernel(EmArgs a) {
             if (a.recv_src_idx != nullptr) a.recv_src_idx[row] = t;
             if (a.recv_weights != nullptr) a.recv_weights[row] = s_coef[warp][lane];
         }
-        if (QUANT)
+        if (QUANT && PAIRS)
+            scatter_quant_pairs_loaded(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
+                                       s_row[warp], nd, a.H, a.qm, lane, qp);
+        else if (QUANT)
             scatter_quant_row_loaded<kQuantU, V32>(src, reinterpret_cast<uint8_t*>(a.recv_x), a.recv_x_scales,
                                                    s_row[warp], nd, a.H, a.qm, lane, 32, 0, qa, qb);
         else
@@ -229,9 +236,11 @@ ep_status ep_dispatch_expert_major(const ep_shape* sh, const void* x, ep_dtype r
         cudaError_t e = cudaSuccess;
         if (recv_dtype == EP_FP8_E4M3) {
             const unsigned blocks = (unsigned)((a.ntok + kWarps - 1) / kWarps);
-            e = ((uintptr_t)x & 31) == 0   // 32-byte loads of the bf16 row
-                    ? launch_pdl(dispatch_em_kernel<true, true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a)
-                    : launch_pdl(dispatch_em_kernel<true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
+            const bool x32 = ((uintptr_t)x & 31) == 0, r32 = ((uintptr_t)out->recv_x & 31) == 0;
+            e = x32 && r32   // 32-byte loads of the bf16 row, 32-byte stores of e4m3 pairs
+                    ? launch_pdl(dispatch_em_kernel<true, true, true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a)
+                : x32 ? launch_pdl(dispatch_em_kernel<true, true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a)
+                      : launch_pdl(dispatch_em_kernel<true>, dim3(blocks), dim3(kThreads), 0, launch->stream, a);
         } else if (tma_smem <= (size_t)kTmaSmemMax) {
             e = cudaFuncSetAttribute(dispatch_em_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kTmaSmemMax);

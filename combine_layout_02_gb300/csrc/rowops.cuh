@@ -3,7 +3,8 @@
 // kernels:
 //   scatter_copy_row   one source row -> nd destination rows (bytes copied)
 //   scatter_quant_row  one bf16 source row -> e4m3 row + per-128-channel fp32 scales,
-//                      quantised once, stored to nd destination rows
+//                      quantised once, stored to nd destination rows (per unit of 16
+//                      channels, or per pair of units with 32-byte stores)
 //   gather_reduce_row  nd bf16 rows * coefficients -> one bf16 row, fp32 accumulation
 // Work is split in 16-byte units: thread `first` handles units first, first+stride, ...
 // Each source byte is loaded once (ld.global.nc, no L1 allocation) and every
@@ -91,6 +92,39 @@ struct QuantMode {
     float tinv;        // 1 / tscale
 };
 
+// The group scale, its inverse and (power-of-two modes) biased exponent byte from the
+// group amax; the per-tensor mode takes the caller's scale and ignores amax.
+__device__ __forceinline__ void quant_scale(float amax, const QuantMode& qm, float& scale, float& inv,
+                                            uint32_t& scale_byte) {
+    scale_byte = 0;
+    if (qm.mode == EP_FP8_SCALE_TENSOR) {
+        scale = qm.tscale;
+        inv = qm.tinv;
+        return;
+    }
+    const float am = fmaxf(amax, 1e-4f);
+    if (qm.mode == EP_FP8_SCALE_FP32) {
+        scale = __fdiv_rn(am, 448.0f);
+        inv = __fdiv_rn(448.0f, am);
+    } else {
+        // s0 >= 1e-4/448 and <= bf16 max/448, so it is a normal number and the rounded-up
+        // power of two and its reciprocal are normal too.
+        const uint32_t bits = __float_as_uint(__fdiv_rn(am, 448.0f));
+        const uint32_t e = ((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) != 0u ? 1u : 0u);
+        scale = __uint_as_float(e << 23);
+        inv = __uint_as_float((254u - e) << 23);
+        scale_byte = e;
+    }
+}
+
+// Four e4m3 values x * inv (round to nearest even, satfinite) packed in a word, the
+// first in the low byte.
+__device__ __forceinline__ uint32_t quant_word(const float* f, float inv) {
+    const uint32_t lo = pack_e4m3x2(__fmul_rn(f[0], inv), __fmul_rn(f[1], inv));
+    const uint32_t hi = pack_e4m3x2(__fmul_rn(f[2], inv), __fmul_rn(f[3], inv));
+    return lo | (hi << 16);
+}
+
 // Quantises one unit (16 bf16 channels held in a, b) to 16 e4m3 bytes. Returns the
 // group scale (fp32) and its biased exponent byte (power-of-two modes).
 __device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, const QuantMode& qm,
@@ -102,40 +136,46 @@ __device__ __forceinline__ uint4 quant_unit(const uint4& a, const uint4& b, cons
         f[2 * j] = bf16_lo(w[j]);
         f[2 * j + 1] = bf16_hi(w[j]);
     }
-    float inv;
-    scale_byte = 0;
-    if (qm.mode == EP_FP8_SCALE_TENSOR) {
-        scale = qm.tscale;
-        inv = qm.tinv;
-    } else {
-        float amax = 0.0f;
+    float amax = 0.0f;
+    if (qm.mode != EP_FP8_SCALE_TENSOR) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
         amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-        const float am = fmaxf(amax, 1e-4f);
-        if (qm.mode == EP_FP8_SCALE_FP32) {
-            scale = __fdiv_rn(am, 448.0f);
-            inv = __fdiv_rn(448.0f, am);
-        } else {
-            // s0 >= 1e-4/448 and <= bf16 max/448, so it is a normal number and the
-            // rounded-up power of two and its reciprocal are normal too.
-            const uint32_t bits = __float_as_uint(__fdiv_rn(am, 448.0f));
-            const uint32_t e = ((bits >> 23) & 0xFFu) + ((bits & 0x7FFFFFu) != 0u ? 1u : 0u);
-            scale = __uint_as_float(e << 23);
-            inv = __uint_as_float((254u - e) << 23);
-            scale_byte = e;
-        }
     }
-    uint32_t qw[4];
+    float inv;
+    quant_scale(amax, qm, scale, inv, scale_byte);
+    return make_uint4(quant_word(f, inv), quant_word(f + 4, inv), quant_word(f + 8, inv),
+                      quant_word(f + 12, inv));
+}
+
+// Quantises a pair of units (32 bf16 channels, two 32-byte loads in v) to 32 e4m3 bytes;
+// 4 consecutive lanes hold a 128-channel group, so the group amax is a 2-step xor-shuffle.
+// Every lane of a warp must call quant_pair together.
+__device__ __forceinline__ u32x8 quant_pair(const u32x8 (&v)[2], const QuantMode& qm, float& scale,
+                                            uint32_t& scale_byte) {
+    float f[32];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = pack_e4m3x2(__fmul_rn(f[4 * j], inv), __fmul_rn(f[4 * j + 1], inv));
-        const uint32_t hi = pack_e4m3x2(__fmul_rn(f[4 * j + 2], inv), __fmul_rn(f[4 * j + 3], inv));
-        qw[j] = lo | (hi << 16);
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            f[16 * h + 2 * j] = bf16_lo(v[h].r[j]);
+            f[16 * h + 2 * j + 1] = bf16_hi(v[h].r[j]);
+        }
+    float amax = 0.0f;
+    if (qm.mode != EP_FP8_SCALE_TENSOR) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     }
-    return make_uint4(qw[0], qw[1], qw[2], qw[3]);
+    float inv;
+    quant_scale(amax, qm, scale, inv, scale_byte);
+    u32x8 q;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) q.r[j] = quant_word(f + 4 * j, inv);
+    return q;
 }
 
 // Stores one quantised unit u (and, for the first unit of a group, its scale: fp32, or
@@ -207,6 +247,51 @@ __device__ __forceinline__ void scatter_quant_row_loaded(const char* __restrict_
             a[i] = na[i];
             b[i] = nb[i];
         }
+    }
+}
+
+// Pair q of a row for quant_pair: 32 bf16 channels (64 bytes) as two 32-byte loads (src
+// 32-byte aligned); zero past the row (those lanes still take part in the shuffles).
+__device__ __forceinline__ void pair_load(const char* __restrict__ src, int pairs, int q, u32x8 (&v)[2]) {
+    if (q < pairs) {
+        v[0] = ld_stream_v8(src + (int64_t)q * 64);
+        v[1] = ld_stream_v8(src + (int64_t)q * 64 + 32);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[0].r[j] = v[1].r[j] = 0u;
+    }
+}
+
+// scatter_quant_row_loaded with pairs: one pair per lane per step, 32-byte loads and one
+// 32-byte store per destination (q_base rows 32-byte aligned); `cur` holds pair `first`,
+// already loaded, and each next pair is loaded before the current one is quantised.
+__device__ __forceinline__ void scatter_quant_pairs_loaded(const char* __restrict__ src,
+                                                           uint8_t* __restrict__ q_base,
+                                                           void* __restrict__ s_base,
+                                                           const int64_t* rows, int nd, int H,
+                                                           const QuantMode& qm, int first,
+                                                           u32x8 (&cur)[2]) {
+    const int pairs = H >> 5, G = H >> 7;
+    for (int q0 = 0; q0 < pairs; q0 += 32) {       // warp-uniform: quant_pair shuffles
+        u32x8 nxt[2];
+        pair_load(src, pairs, q0 + 32 + first, nxt);
+        float scale;
+        uint32_t sbyte;
+        const u32x8 qv = quant_pair(cur, qm, scale, sbyte);
+        const int q = q0 + first;
+        if (q < pairs) {
+            for (int p = 0; p < nd; ++p) {
+                st_v8(q_base + rows[p] * (int64_t)H + (int64_t)q * 32, qv);
+                if ((q & 3) == 0) {
+                    if (qm.mode == EP_FP8_SCALE_UE8M0)
+                        reinterpret_cast<uint8_t*>(s_base)[rows[p] * (int64_t)G + (q >> 2)] = (uint8_t)sbyte;
+                    else
+                        reinterpret_cast<float*>(s_base)[rows[p] * (int64_t)G + (q >> 2)] = scale;
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) cur[h] = nxt[h];
     }
 }
 

@@ -648,3 +648,42 @@ def test_ll_repeated_experts_across_rank_chunks(packed, E):
     filled = exp["src_info"] != -7
     np.testing.assert_array_equal(host_bits(buf.recv_x)[filled], exp["recv_x"][filled])
     assert run.flags() == 0
+
+
+@pytest.mark.parametrize("name", ["h16k", "group8"])
+def test_fp8_receive_rows_16_byte_aligned(name):
+    """Fused e4m3 into receive rows that are 16- but not 32-byte aligned (the 32-byte-store
+    pair form then falls back to 16-byte stores), rank-major and expert-major, against the
+    oracle; and into aligned rows (the pair form where it applies)."""
+    w, inp, run, ref = _setup(name)
+    run.layout()
+    off = compact_offsets(ref["rank_prefix_matrix"])
+    G = w.H // 128
+    exp = oracle.dispatch(inp["x"], ref["send_head"], np.array(off), w.E, x_kind=oracle.X_QUANTIZE)
+    for shift in (0, 16):
+        qbuf = torch.zeros(off[-1] * w.H + 32, dtype=torch.uint8, device="cuda")
+        rq = qbuf[shift: shift + off[-1] * w.H].view(off[-1], w.H)
+        assert rq.data_ptr() % 32 == shift
+        rs = torch.zeros((off[-1], G), dtype=torch.float32, device="cuda")
+        ep.ep_dispatch(run.sh, run.x, ep.EP_BF16, None, ep.EP_FP8_E4M3, None, None,
+                       run.lb.handle(), rq, rs, None, None, None, off, run.launch)
+        np.testing.assert_array_equal(host_bits(rq), exp["recv_x"], err_msg=f"shift {shift}")
+        np.testing.assert_array_equal(host_bits(rs).view(np.uint32), exp["recv_x_scales"].view(np.uint32))
+    from combine_layout_02_gb300.buffers import LayoutBuffers
+    lb = LayoutBuffers(run.sh, expert_major=True)
+    ep.ep_get_layout(run.sh, run.topk, lb.layout(), lb.handle(), lb.workspace, run.launch)
+    em = oracle.expert_layout(inp["topk_idx"], w.E)
+    eoff = [0]
+    for n in em["expert_prefix"][:, -1]:
+        eoff.append(eoff[-1] + int(n))
+    ee = oracle.dispatch_expert_major(inp["x"], inp["topk_idx"], inp["topk_weights"], em["expert_rows"],
+                                      np.array(eoff), w.E, quantize=True)
+    for shift in (0, 16):
+        ebuf = torch.zeros(eoff[-1] * w.H + 32, dtype=torch.uint8, device="cuda")
+        rx = ebuf[shift: shift + eoff[-1] * w.H].view(eoff[-1], w.H)
+        rs = torch.zeros((eoff[-1], G), dtype=torch.float32, device="cuda")
+        ep.ep_dispatch_expert_major(run.sh, run.x, ep.EP_FP8_E4M3, run.topk, run.wts, lb.handle(), rx, rs,
+                                    None, None, eoff, run.launch)
+        np.testing.assert_array_equal(host_bits(rx), ee["recv_x"], err_msg=f"expert-major shift {shift}")
+        np.testing.assert_array_equal(host_bits(rs).view(np.uint32), ee["recv_x_scales"].view(np.uint32))
+    assert run.flags() == 0
