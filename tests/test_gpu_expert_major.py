@@ -2,8 +2,9 @@
 local expert, then source rank, then token) against the oracle: the handle's
 expert_rows / expert_prefix bit-exact on shapes that exercise every bitmask width
 (E from 4 to 4096), dispatch rows / scales / metadata bit-exact (bf16, e4m3 with every
-scale format), combine within 1e-3 absolute + 1e-2 relative, and the dsv3 shape at full
-size with exact receive regions."""
+scale format), combine within 1e-3 absolute + 1e-2 relative on every combine form (rows of
+at most 256 channels, up to 1024, at most two rows per token, the rest), and the dsv3 shape
+at full size with exact receive regions."""
 import ctypes
 
 import numpy as np
@@ -30,6 +31,8 @@ CASES = {
     "k32": W("emk", R=8, T=64, H=128, E=64, k=32, C=3, seed=306),
     "e1024": W("em1k", R=8, T=200, H=128, E=1024, k=8, C=4, seed=307),
     "e4096": W("em4k", R=16, T=100, H=128, E=4096, k=8, C=3, seed=308),
+    "top2_h2048": W("em2", R=8, T=200, H=2048, E=64, k=2, C=4, seed=309),     # <= 2 rows per token
+    "h4096": W("em4", R=4, T=100, H=4096, E=16, k=4, C=3, seed=310),           # wide rows, k > 2
 }
 
 
@@ -96,7 +99,8 @@ def test_expert_layout_bit_exact(name):
     assert run.flags() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf16", "group8", "k32", "e4096"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf16", "group8", "k32", "e4096", "top2_h2048",
+                                  "h4096"])
 def test_dispatch_expert_major_bf16_bit_exact(name):
     w, inp, run, ref, off = _setup(name)
     rx, _, rw, ri = run.dispatch(off)
@@ -108,7 +112,7 @@ def test_dispatch_expert_major_bf16_bit_exact(name):
     assert run.flags() == 0
 
 
-@pytest.mark.parametrize("name", ["tiny", "group8"])
+@pytest.mark.parametrize("name", ["tiny", "group8", "h4096"])
 @pytest.mark.parametrize("mode,ts", [(0, 0.0), (1, 0.0), (2, 0.0), (3, 0.0173)])
 def test_dispatch_expert_major_fp8_bit_exact(name, mode, ts):
     w, inp, run, ref, off = _setup(name)
@@ -123,7 +127,7 @@ def test_dispatch_expert_major_fp8_bit_exact(name, mode, ts):
         np.testing.assert_array_equal(host_bits(rs).view(np.uint32), exp["recv_x_scales"].view(np.uint32))
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf16", "group8", "k32"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "zipf16", "group8", "k32", "top2_h2048", "h4096"])
 @pytest.mark.parametrize("mode", [ep.EP_COMBINE_SUM, ep.EP_COMBINE_WEIGHTED])
 def test_combine_expert_major_within_tolerance(name, mode):
     w, inp, run, ref, off = _setup(name)
