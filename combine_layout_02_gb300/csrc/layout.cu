@@ -542,8 +542,9 @@ ep_status ep_get_layout(const ep_shape* sh, const int64_t* topk_idx, ep_layout* 
     a.ws_etot = a.ws_expert + (size_t)a.R * a.C * a.E;
     a.expert_rows = handle->expert_rows;
     a.expert_prefix = handle->expert_prefix;
-    // Bitmask words per expert (rows padded to an odd stride): at most ~6144 + E words.
-    a.ew = expert ? (a.E >= 6144 ? 1 : (6144 / a.E > 16 ? 16 : 6144 / a.E)) : 1;
+    // Bitmask words per expert (rows padded to an odd stride): at most ~6144 + E words. A
+    // sub-tile of 32 * ew tokens has one thread per token, so ew <= kWarps.
+    a.ew = expert ? (a.E >= 6144 ? 1 : (6144 / a.E > kWarps ? kWarps : 6144 / a.E)) : 1;
     a.err = launch->error_flags;
 
     a.el_shift = (a.E_loc & (a.E_loc - 1)) == 0 ? __builtin_ctz((unsigned)a.E_loc) : -1;
